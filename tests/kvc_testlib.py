@@ -1,0 +1,84 @@
+"""Helpers shared by the tests: a brute-force decoder of the packed kv_cache
+slot layout and bf16 conversions through torch (a library routine).
+
+Layout ("Gather and Scatter" and "How One Output Is Produced" of the
+KernelGen Challenge 8 write-up): a page holds 64 slots; slot ``off`` of page
+``pg`` keeps 576 payload bytes at ``[pg, off*576]`` -- 448 int8 NOPE codes then
+64 little-endian bf16 RoPE values -- and 8 scale bytes at
+``[pg, 64*576 + off*8]``: 7 exponent bytes ``e + 127`` and one padding byte.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+PAGE_SLOTS = 64
+TOKEN_STRIDE = 576
+SCALE_DIM = 8
+PAGE_BYTES = PAGE_SLOTS * (TOKEN_STRIDE + SCALE_DIM)
+SCALE_BASE = PAGE_SLOTS * TOKEN_STRIDE
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def torch_bf16_bits(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def slot_byte_ranges(slot: int):
+    """(payload_start, scale_start) flat byte offsets of ``slot`` in kv_cache."""
+    pg, off = divmod(int(slot), PAGE_SLOTS)
+    return pg * PAGE_BYTES + off * TOKEN_STRIDE, pg * PAGE_BYTES + SCALE_BASE + off * SCALE_DIM
+
+
+def decode_slot(kv: np.ndarray, slot: int):
+    """Read one slot back: (q int8[448], e int[7], pad byte, rope f32[64])."""
+    flat = kv.reshape(-1)
+    p0, s0 = slot_byte_ranges(slot)
+    payload = flat[p0:p0 + TOKEN_STRIDE]
+    scale = flat[s0:s0 + SCALE_DIM]
+    q = payload[:448].view(np.int8).astype(np.int64)
+    e = scale[:7].astype(np.int64) - 127
+    rope_bits = payload[448:].copy().view("<u2")
+    return q, e, int(scale[7]), bf16_bits_to_f32(rope_bits)
+
+
+def dequant(q: np.ndarray, e: np.ndarray) -> np.ndarray:
+    """NOPE values back from codes: q * 2^e, per 64-dim group (float64)."""
+    return q.astype(np.float64) * np.repeat(np.ldexp(1.0, e), 64)
+
+
+def written_mask(kv_shape, slots) -> np.ndarray:
+    """Boolean mask (flat) of the bytes owned by the given slots."""
+    m = np.zeros(int(np.prod(kv_shape)), dtype=bool)
+    for s in slots:
+        if s < 0:
+            continue
+        p0, s0 = slot_byte_ranges(s)
+        m[p0:p0 + TOKEN_STRIDE] = True
+        m[s0:s0 + SCALE_DIM] = True
+    return m
+
+
+def slots_of_case(case) -> np.ndarray:
+    """Slot written by each output n (kv_slot_mapping indexed by token)."""
+    return case.kv_slot_mapping[case.boundary_token_indices]
+
+
+def gather_window_rows(case) -> np.ndarray:
+    """The page's baseline gather: flat row ids [N, C] through block_table.
+
+    Restates "The Baseline" (flat_idx = block_numbers * block_size +
+    block_offsets) in numpy, for the torch cross-check of the reduction.
+    """
+    B, C = case.block_size, case.compress_ratio
+    b = case.boundary_token_indices
+    r = case.token_to_req[b].astype(np.int64)
+    p = case.positions[b]
+    t = p[:, None] - C + 1 + np.arange(C)[None, :]
+    blk = case.block_table[r[:, None], t // B].astype(np.int64)
+    return blk * B + t % B
