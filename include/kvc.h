@@ -1,0 +1,135 @@
+/*
+ * kvc.h -- C ABI of the GB300 KV-cache window compressor.
+ *
+ * The operator is c128_256_512_compress from "From Attention to KV Cache
+ * Compression: Notes from a KernelGen Optimization" (KernelGen Challenge 8
+ * write-up): section "The Compression Operator" gives the argument list,
+ * "Gather and Scatter" the constants and the packed slot layout, and "How
+ * One Output Is Produced" the computation:
+ *
+ *   for every boundary token b = boundary_token_indices[n]:
+ *     r = token_to_req[b], p = positions[b], window t = p-C+1 .. p;
+ *     row(t) = block_table[r, t/8] * 8 + t%8 of state_cache (block_size 8);
+ *     c_d = sum_t softmax_t(score[row(t), d]) * value[row(t), d], d < 512
+ *           (softmax along the window, separately per dimension);
+ *     y = c * (mean(c^2) + eps)^-1/2 * rms_norm_weight;
+ *     dims 0..447: z = bf16(y); per 64-dim group a = max(max|z|, 1e-4),
+ *       e = ceil(log2(a/127)), q = trunc(z * 2^-e) clipped to +-127 (int8),
+ *       scale byte = e + 127;
+ *     dims 448..511: GPT-J interleaved RoPE with the cos/sin row
+ *       pc = floor(p/C)*C, stored as bf16;
+ *     slot = kv_slot_mapping[b]: 576 payload bytes at
+ *       kv_cache[slot/64, (slot%64)*576] and 8 scale bytes (7 exponents + a
+ *       zero padding byte) at kv_cache[slot/64, 64*576 + (slot%64)*8].
+ *
+ * All pointers name device memory of the current CUDA device unless stated
+ * otherwise; the caller owns every buffer.  Calls are asynchronous on the
+ * given stream and never synchronise it (kvc_get_device_error excepted).
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVC_OK = 0,
+  KVC_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, small workspace */
+  KVC_ERR_UNSUPPORTED = 2,  /* block_size != 8, C not a multiple of 8, or (device)
+                               a window that does not start on an 8-row block */
+  KVC_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  KVC_ERR_BAD_INDEX = 4,    /* (device) an index outside its array */
+  KVC_ERR_TIMEOUT = 5       /* (device) a pipeline wait ran past its limit */
+} kvc_status;
+
+/* flags: bits 0..15 force the number of CTAs of the launch (0 = automatic:
+ * one or two persistent CTAs per SM).  Other bits must be zero. */
+#define KVC_FLAG_GRID_MASK 0xFFFFu
+
+/*
+ * Bytes of device workspace kvc_compress needs for num_outputs outputs on
+ * the current device.  The workspace holds the partial softmax states of
+ * outputs whose window is split between two or more CTAs and one arrival
+ * counter per output.  Returns 0 on error (no CUDA device).
+ */
+size_t kvc_workspace_bytes(int64_t num_outputs);
+
+/*
+ * Compress every boundary token's window into its kv_cache slot.
+ *
+ * state_cache      bf16 [num_state_blocks, 8, 1024], contiguous, 16-byte
+ *                  aligned; row columns 0..511 are values, 512..1023 scores.
+ * token_to_req     int32 [num_tokens]: request of each token.
+ * positions        int64 [num_tokens]: position of each token in its request.
+ * boundary_token_indices  int64 [num_outputs]: token index b of each output.
+ * block_table      int32 [num_reqs, max_blocks_per_req] (row stride
+ *                  max_blocks_per_req): physical block of each logical block.
+ * rms_norm_weight  fp32 [512].
+ * cos_sin_cache    fp32 [num_positions, 64]: cos in columns 0..31, sin 32..63.
+ * kv_slot_mapping  int64: indexed by token (slot_mapping_len == num_tokens)
+ *                  or by output (slot_mapping_len == num_outputs).  A
+ *                  negative slot skips that output.
+ * kv_cache         uint8 [num_kv_pages, 37376], 16-byte aligned; written in
+ *                  place, only at the 576 + 8 bytes of each written slot.
+ * block_size       must be 8.   compress_ratio  C, a positive multiple of 8.
+ * rms_norm_eps     finite, >= 0 (the write-up's default is 1e-6).
+ * y_out            optional fp32 [num_outputs, 512], 8-byte aligned, or NULL:
+ *                  receives the RMS-normalised vector y of each output (before
+ *                  the bf16 rounding, quantisation and RoPE).
+ * workspace        device buffer of at least kvc_workspace_bytes(num_outputs)
+ *                  bytes, 16-byte aligned, ZERO-FILLED before its first use.
+ *                  Every completed call leaves its counters at zero again, so
+ *                  one workspace serves any number of calls in stream order.
+ *                  Calls that may run concurrently need separate workspaces.
+ * stream           cudaStream_t (NULL = legacy default stream).
+ *
+ * Host-detected errors return before anything is launched.  Device-detected
+ * errors (an index outside its array, a window that starts before position
+ * 0 or off an 8-row block boundary) never trap: the offending output's slot
+ * is left untouched, the other outputs are written, and a sticky device
+ * error code is recorded for kvc_get_device_error.
+ */
+kvc_status kvc_compress(
+    const void* state_cache, int64_t num_state_blocks,
+    const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
+    const int64_t* boundary_token_indices, int64_t num_outputs,
+    const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    const float* rms_norm_weight,
+    const float* cos_sin_cache, int64_t num_positions,
+    const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+    uint8_t* kv_cache, int64_t num_kv_pages,
+    int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
+    float* y_out, void* workspace, size_t workspace_bytes,
+    uint32_t flags, void* stream);
+
+/*
+ * Launch shape kvc_compress would use for this problem on the current
+ * device: CTAs, threads per CTA and dynamic shared memory bytes.  Any out
+ * pointer may be NULL.  flags as for kvc_compress.
+ */
+kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio,
+                            uint32_t flags, int32_t* ctas, int32_t* threads,
+                            int32_t* smem_bytes);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error code
+ * recorded by kernels of this library on the current device (KVC_OK if
+ * none).  The code is the first one recorded since the last clear.
+ */
+kvc_status kvc_get_device_error(void* stream, uint32_t* out_code);
+
+/* Static description of a status code. */
+const char* kvc_error_string(kvc_status status);
+
+/* Library identification: version, target architecture and kernel route. */
+const char* kvc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */

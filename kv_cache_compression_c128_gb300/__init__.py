@@ -1,0 +1,272 @@
+"""GB300-native KV-cache window compressor (``c128_256_512_compress``).
+
+The computation runs in the CUDA library ``_lib/libkvc.so`` (sources in
+``csrc/``, C ABI in ``include/kvc.h``); this module only marshals arguments
+through ctypes.  There is no CPU fallback: if the library is missing or no
+CUDA device is present, the calls raise.
+
+The operator is the one of "From Attention to KV Cache Compression: Notes
+from a KernelGen Optimization" (KernelGen Challenge 8 write-up), section
+"The Compression Operator", with the layout of "Gather and Scatter".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_CSRC = os.path.join(_HERE, "csrc")
+_INCLUDE = os.path.join(_ROOT, "include")
+_LIB_DIR = os.path.join(_HERE, "_lib")
+LIB_PATH = os.path.join(_LIB_DIR, "libkvc.so")
+_SOURCES = ["kvc_compress.cu", "kvc_api.cu"]
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+KVC_OK = 0
+KVC_ERR_INVALID_ARG = 1
+KVC_ERR_UNSUPPORTED = 2
+KVC_ERR_CUDA = 3
+KVC_ERR_BAD_INDEX = 4
+KVC_ERR_TIMEOUT = 5
+KVC_FLAG_GRID_MASK = 0xFFFF
+
+HEAD_DIM = 512
+KV_PAGE_BYTES = 64 * (576 + 8)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KvcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kvc_error_string(status)} (status {status})")
+
+
+# ---- build -------------------------------------------------------------------
+
+def _nvcc() -> str:
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    deps = [os.path.join(_CSRC, f) for f in os.listdir(_CSRC)]
+    deps.append(os.path.join(_INCLUDE, "kvc.h"))
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a into _lib/libkvc.so (in-tree)."""
+    if not force and not _stale():
+        return LIB_PATH
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    nvcc = _nvcc()
+    common = ARCH_FLAGS + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+                           "-I", _INCLUDE]
+    objs = [os.path.join(_LIB_DIR, s.replace(".cu", ".o")) for s in _SOURCES]
+
+    def compile_one(src_obj):
+        src, obj = src_obj
+        cmd = [nvcc] + common + ["-c", os.path.join(_CSRC, src), "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return r.stderr
+
+    with ThreadPoolExecutor(len(_SOURCES)) as ex:
+        logs = list(ex.map(compile_one, zip(_SOURCES, objs)))
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, "-shared"] + ARCH_FLAGS + objs + ["-o", tmp],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB_PATH)
+    if verbose:
+        print("".join(logs))
+    return LIB_PATH
+
+
+# ---- loading -----------------------------------------------------------------
+
+def lib():
+    """The loaded libkvc.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "kv_cache_compression_c128_gb300.build() (there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, I32, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+            L.kvc_workspace_bytes.argtypes = [I64]
+            L.kvc_workspace_bytes.restype = ctypes.c_size_t
+            L.kvc_compress.argtypes = [
+                P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P, I64,
+                I32, I32, ctypes.c_float, P, P, ctypes.c_size_t, U32, P]
+            L.kvc_compress.restype = ctypes.c_int
+            L.kvc_query_launch.argtypes = [I64, I32, U32, P, P, P]
+            L.kvc_query_launch.restype = ctypes.c_int
+            L.kvc_get_device_error.argtypes = [P, P]
+            L.kvc_get_device_error.restype = ctypes.c_int
+            L.kvc_error_string.argtypes = [ctypes.c_int]
+            L.kvc_error_string.restype = ctypes.c_char_p
+            L.kvc_version.argtypes = []
+            L.kvc_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+# ---- the C ABI, one Python function per entry point ---------------------------
+
+def kvc_error_string(status: int) -> str:
+    return lib().kvc_error_string(int(status)).decode()
+
+
+def kvc_version() -> str:
+    return lib().kvc_version().decode()
+
+
+def kvc_workspace_bytes(num_outputs: int) -> int:
+    return int(lib().kvc_workspace_bytes(int(num_outputs)))
+
+
+def kvc_query_launch(num_outputs: int, compress_ratio: int, flags: int = 0):
+    """(ctas, threads, dynamic smem bytes) of the launch for this problem."""
+    c, t, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    st = lib().kvc_query_launch(int(num_outputs), int(compress_ratio), int(flags),
+                                ctypes.byref(c), ctypes.byref(t), ctypes.byref(s))
+    if st != KVC_OK:
+        raise KvcError(st, "kvc_query_launch")
+    return c.value, t.value, s.value
+
+
+def kvc_get_device_error(stream: Optional[int] = None) -> int:
+    """Synchronise `stream` (a cudaStream_t as int), read and clear the
+    device error code."""
+    code = ctypes.c_uint32()
+    st = lib().kvc_get_device_error(ctypes.c_void_p(stream or 0), ctypes.byref(code))
+    if st != KVC_OK:
+        raise KvcError(st, "kvc_get_device_error")
+    return int(code.value)
+
+
+def kvc_compress(state_cache, num_state_blocks, token_to_req, positions, num_tokens,
+                 boundary_token_indices, num_outputs, block_table, num_reqs,
+                 max_blocks_per_req, rms_norm_weight, cos_sin_cache, num_positions,
+                 kv_slot_mapping, slot_mapping_len, kv_cache, num_kv_pages, block_size,
+                 compress_ratio, rms_norm_eps, y_out, workspace, workspace_bytes,
+                 flags, stream) -> int:
+    """The C entry point with raw integer pointers; returns the status."""
+    v = ctypes.c_void_p
+    return int(lib().kvc_compress(
+        v(state_cache), num_state_blocks, v(token_to_req), v(positions), num_tokens,
+        v(boundary_token_indices), num_outputs, v(block_table), num_reqs,
+        max_blocks_per_req, v(rms_norm_weight), v(cos_sin_cache), num_positions,
+        v(kv_slot_mapping), slot_mapping_len, v(kv_cache), num_kv_pages, block_size,
+        compress_ratio, ctypes.c_float(rms_norm_eps), v(y_out), v(workspace),
+        workspace_bytes, flags, v(stream)))
+
+
+# ---- torch-facing wrapper with the statement's signature ----------------------
+
+_workspaces = {}
+
+
+def workspace_for(device, stream_ptr: int, num_outputs: int):
+    """A zero-initialised workspace cached per (device, stream)."""
+    import torch
+
+    need = kvc_workspace_bytes(num_outputs)
+    key = (device.index, stream_ptr)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def _check(t, name, dtype, device):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def c128_256_512_compress(state_cache, token_to_req, positions, boundary_token_indices,
+                          block_table, rms_norm_weight, cos_sin_cache, kv_slot_mapping,
+                          kv_cache, block_size, compress_ratio, rms_norm_eps=1.0e-6, *,
+                          y_out=None, flags: int = 0, stream=None, workspace=None):
+    """Compress every boundary token's window into its kv_cache slot, in place.
+
+    state_cache bf16 [blocks, 8, 1024]; token_to_req int32 [T]; positions
+    int64 [T]; boundary_token_indices int64 [N]; block_table int32 [R, Lb];
+    rms_norm_weight fp32 [512]; cos_sin_cache fp32 [P, 64]; kv_slot_mapping
+    int64 [T] (or [N]); kv_cache uint8 [pages, 37376].  All on one CUDA
+    device.  Optional y_out fp32 [N, 512] receives the normalised vectors.
+    Returns kv_cache.
+    """
+    import torch
+
+    dev = state_cache.device
+    if dev.type != "cuda":
+        raise ValueError("state_cache must be a CUDA tensor (there is no CPU path)")
+    _check(state_cache, "state_cache", torch.bfloat16, dev)
+    _check(token_to_req, "token_to_req", torch.int32, dev)
+    _check(positions, "positions", torch.int64, dev)
+    _check(boundary_token_indices, "boundary_token_indices", torch.int64, dev)
+    _check(block_table, "block_table", torch.int32, dev)
+    _check(rms_norm_weight, "rms_norm_weight", torch.float32, dev)
+    _check(cos_sin_cache, "cos_sin_cache", torch.float32, dev)
+    _check(kv_slot_mapping, "kv_slot_mapping", torch.int64, dev)
+    _check(kv_cache, "kv_cache", torch.uint8, dev)
+    if state_cache.dim() != 3 or state_cache.shape[2] != 2 * HEAD_DIM:
+        raise ValueError("state_cache must be [num_blocks, block_size, 1024]")
+    if state_cache.shape[1] != block_size:
+        raise ValueError("state_cache.shape[1] must equal block_size")
+    if block_table.dim() != 2 or cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != 64:
+        raise ValueError("block_table must be 2-D and cos_sin_cache [P, 64]")
+    if rms_norm_weight.numel() != HEAD_DIM:
+        raise ValueError("rms_norm_weight must have 512 elements")
+    if kv_cache.dim() != 2 or kv_cache.shape[1] != KV_PAGE_BYTES:
+        raise ValueError(f"kv_cache must be [num_pages, {KV_PAGE_BYTES}] uint8")
+    if token_to_req.numel() != positions.numel():
+        raise ValueError("token_to_req and positions must have one entry per token")
+    N = boundary_token_indices.numel()
+    if y_out is not None:
+        _check(y_out, "y_out", torch.float32, dev)
+        if y_out.numel() < N * HEAD_DIM:
+            raise ValueError("y_out must hold num_outputs * 512 floats")
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        sp = int(s.cuda_stream)
+        ws = workspace if workspace is not None else workspace_for(dev, sp, N)
+        st = kvc_compress(
+            state_cache.data_ptr(), state_cache.shape[0], token_to_req.data_ptr(),
+            positions.data_ptr(), positions.numel(), boundary_token_indices.data_ptr(), N,
+            block_table.data_ptr(), block_table.shape[0], block_table.shape[1],
+            rms_norm_weight.data_ptr(), cos_sin_cache.data_ptr(), cos_sin_cache.shape[0],
+            kv_slot_mapping.data_ptr(), kv_slot_mapping.numel(), kv_cache.data_ptr(),
+            kv_cache.shape[0], int(block_size), int(compress_ratio), float(rms_norm_eps),
+            0 if y_out is None else y_out.data_ptr(), ws.data_ptr(), ws.numel(),
+            int(flags), sp)
+    if st != KVC_OK:
+        raise KvcError(st, "kvc_compress")
+    return kv_cache

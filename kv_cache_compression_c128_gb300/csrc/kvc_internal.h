@@ -1,0 +1,78 @@
+// Internal interface between the C ABI layer (kvc_api.cu) and the fused
+// kernel (kvc_compress.cu).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace kvc {
+
+// Constants of the section "Gather and Scatter" of the KernelGen Challenge 8
+// write-up, plus the paged state geometry (block_size 8, 512 values + 512
+// scores per row).
+constexpr int kHeadDim = 512;
+constexpr int kNopeDim = 448;
+constexpr int kRopeDim = 64;
+constexpr int kGroup = 64;
+constexpr int kRowElems = 2 * kHeadDim;                    // bf16 per state row
+constexpr int kBlockRows = 8;                              // block_size
+constexpr int kBlockBytes = kBlockRows * kRowElems * 2;    // 16 KiB per block
+constexpr int kSlotsPerPage = 64;
+constexpr int kTokenStride = 576;
+constexpr int kScaleDim = 8;
+constexpr int64_t kPageBytes = kSlotsPerPage * (kTokenStride + kScaleDim);
+constexpr int kScaleBase = kSlotsPerPage * kTokenStride;   // 36864
+
+// CTA shape: 8 consumer warps (thread t owns dims 2t, 2t+1) + 1 producer warp.
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kStages = 6;                                 // 16 KiB ring stages
+constexpr int kMetaRing = kStages + 2;                     // per-output records
+
+// A split output's partial softmax state: m[512], den[512], num[512].
+constexpr int kPartialFloats = 3 * kHeadDim;
+
+struct Params {
+  const uint16_t* state;          // bf16 bits [num_blocks, 8, 1024]
+  int64_t num_blocks;
+  const int32_t* token_to_req;
+  const int64_t* positions;
+  int64_t num_tokens;
+  const int64_t* bti;             // boundary_token_indices
+  int64_t num_outputs;
+  const int32_t* block_table;
+  int64_t num_reqs;
+  int64_t max_blocks;
+  const float* weight;
+  const float* cos_sin;
+  int64_t num_positions;
+  const int64_t* slot_map;
+  int slot_by_token;              // 1: slot_map[b], 0: slot_map[n]
+  uint8_t* kv;
+  int64_t num_pages;
+  float* y_out;                   // optional
+  int compress_ratio;             // C
+  int blocks_per_output;          // K = C / 8
+  int64_t num_units;              // U = N * K: one unit = one 8-row block
+  float eps;
+  float* partials;                // [2 * max_ctas][kPartialFloats]
+  int32_t* part_status;           // [2 * max_ctas]
+  int32_t* counters;              // [num_outputs]
+  uint32_t* error;                // device error word
+};
+
+// Workspace layout (byte offsets), given the device's CTA capacity.
+struct WorkspaceLayout {
+  size_t partials, status, counters, total;
+};
+WorkspaceLayout workspace_layout(int max_ctas, int64_t num_outputs);
+
+size_t dynamic_smem_bytes();
+const void* kernel_symbol();
+uint32_t* device_error_word();     // device address of the error word (per device)
+cudaError_t launch(const Params& p, int ctas, cudaStream_t stream);
+
+}  // namespace kvc

@@ -82,3 +82,36 @@ def gather_window_rows(case) -> np.ndarray:
     t = p[:, None] - C + 1 + np.arange(C)[None, :]
     blk = case.block_table[r[:, None], t // B].astype(np.int64)
     return blk * B + t % B
+
+
+# ---- running a case through the CUDA library (GPU tests) --------------------
+
+def to_device(case, device="cuda"):
+    """The case's arrays as torch tensors on `device` (kv_cache copied)."""
+    st = torch.from_numpy(case.state_bits.view(np.int16)).view(torch.bfloat16)
+    return dict(
+        state_cache=st.to(device),
+        token_to_req=torch.from_numpy(case.token_to_req).to(device),
+        positions=torch.from_numpy(case.positions).to(device),
+        boundary_token_indices=torch.from_numpy(case.boundary_token_indices).to(device),
+        block_table=torch.from_numpy(case.block_table).to(device),
+        rms_norm_weight=torch.from_numpy(case.rms_norm_weight).to(device),
+        cos_sin_cache=torch.from_numpy(case.cos_sin_cache).to(device),
+        kv_slot_mapping=torch.from_numpy(case.kv_slot_mapping).to(device),
+        kv_cache=torch.from_numpy(case.kv_cache.copy()).to(device),
+    )
+
+
+def run_gpu(case, flags=0, dev_arrays=None, slot_mapping=None):
+    """Run the CUDA library on a case; returns (kv np, y np, device error)."""
+    import kv_cache_compression_c128_gb300 as kvc
+
+    d = dev_arrays if dev_arrays is not None else to_device(case)
+    if slot_mapping is not None:
+        d = dict(d, kv_slot_mapping=torch.from_numpy(slot_mapping).to(d["kv_cache"].device))
+    N = case.num_outputs
+    y = torch.full((max(N, 1), 512), float("nan"), dtype=torch.float32, device=d["kv_cache"].device)
+    kvc.c128_256_512_compress(block_size=case.block_size, compress_ratio=case.compress_ratio,
+                              rms_norm_eps=case.rms_norm_eps, y_out=y, flags=flags, **d)
+    err = kvc.kvc_get_device_error(torch.cuda.current_stream().cuda_stream)
+    return d["kv_cache"].cpu().numpy(), y[:N].cpu().numpy(), err

@@ -1,0 +1,120 @@
+"""C-ABI checks that need no GPU.
+
+The library is compiled for sm_103a on the CPU machine (nvcc cross-compiles),
+loaded with ctypes, and checked to export every function include/kvc.h
+declares.  Every argument check kvc_compress performs on the host happens
+before any CUDA call, so the error paths run here too.
+"""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import kv_cache_compression_c128_gb300 as kvc
+
+    kvc.build()
+    return kvc
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "kvc.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvc_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    assert {"kvc_compress", "kvc_workspace_bytes", "kvc_get_device_error",
+            "kvc_error_string", "kvc_version", "kvc_query_launch"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(kvc):
+    lib = ctypes.CDLL(kvc.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in kvc.h but not exported"
+
+
+def test_library_is_built_for_sm_103a(kvc):
+    # the fatbin carries an sm_103a cubin: the ELF note lists the arch name
+    with open(kvc.LIB_PATH, "rb") as f:
+        blob = f.read()
+    assert b"sm_103a" in blob or b"sm_103" in blob
+
+
+def test_strings(kvc):
+    assert kvc.kvc_error_string(0) == "ok"
+    assert "index" in kvc.kvc_error_string(4)
+    assert kvc.kvc_error_string(99) == "unknown status"
+    assert "sm_103a" in kvc.kvc_version()
+
+
+# a valid-looking argument set; pointers are fake (never dereferenced on the
+# host, and every case below is rejected before any CUDA call)
+_GOOD = dict(state_cache=0x10000, num_state_blocks=1024, token_to_req=0x20000,
+             positions=0x30000, num_tokens=8192, boundary_token_indices=0x40000,
+             num_outputs=64, block_table=0x50000, num_reqs=1, max_blocks_per_req=1024,
+             rms_norm_weight=0x60000, cos_sin_cache=0x70000, num_positions=8192,
+             kv_slot_mapping=0x80000, slot_mapping_len=8192, kv_cache=0x90000,
+             num_kv_pages=1, block_size=8, compress_ratio=128, rms_norm_eps=1e-6,
+             y_out=0, workspace=0xA0000, workspace_bytes=1 << 24, flags=0, stream=0)
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(block_size=16), 2),
+    (dict(compress_ratio=100), 2),
+    (dict(compress_ratio=0), 2),
+    (dict(num_outputs=-1), 1),
+    (dict(flags=1 << 20), 1),
+    (dict(rms_norm_eps=float("nan")), 1),
+    (dict(rms_norm_eps=-1.0), 1),
+    (dict(state_cache=0), 1),
+    (dict(kv_cache=0), 1),
+    (dict(workspace=0), 1),
+    (dict(num_kv_pages=0), 1),
+    (dict(slot_mapping_len=77), 1),
+    (dict(state_cache=0x10008), 1),      # not 16-byte aligned
+    (dict(kv_cache=0x90004), 1),
+    (dict(positions=0x30004), 1),
+    (dict(y_out=0xB0004), 1),
+])
+def test_host_argument_validation(kvc, change, status):
+    args = dict(_GOOD, **change)
+    assert kvc.kvc_compress(**args) == status
+
+
+def test_zero_outputs_is_a_no_op(kvc):
+    assert kvc.kvc_compress(**dict(_GOOD, num_outputs=0)) == 0
+
+
+def test_query_launch_rejects_bad_arguments(kvc):
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_query_launch(64, 100)
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_query_launch(-1, 128)
+
+
+def test_torch_wrapper_rejects_cpu_tensors(kvc):
+    import torch
+
+    from kv_cache_compression_c128_gb300 import inputs
+
+    case = inputs.make_case(1, 256, 16, seed=1)
+    st = torch.from_numpy(case.state_bits.view("int16")).view(torch.bfloat16)
+    t = torch.from_numpy
+    with pytest.raises(ValueError, match="no CPU path"):
+        kvc.c128_256_512_compress(st, t(case.token_to_req), t(case.positions),
+                                  t(case.boundary_token_indices), t(case.block_table),
+                                  t(case.rms_norm_weight), t(case.cos_sin_cache),
+                                  t(case.kv_slot_mapping), t(case.kv_cache), 8, 16)
