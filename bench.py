@@ -1,0 +1,487 @@
+"""Benchmark of the fused KV-cache window compressor on one GB300 (or N).
+
+One step = one call of the whole operator (gather, window reduce, RMSNorm,
+quantisation, RoPE, scatter) over the largest benchmark shape of the
+KernelGen Challenge 8 write-up: 8 requests x 16384 tokens, compress_ratio
+128, block_size 8 (1024 outputs, 256 MiB of bf16 state).  The line printed
+is the operator's effective HBM bandwidth (algorithmic bytes / time).
+
+Timing: inputs resident in HBM; the state is rotated over >= 3 copies whose
+total size is several times the L2, so no call reads what the previous one
+left in L2; the K timed launches are replayed from CUDA graphs and timed
+with CUDA events on the launching stream, between device synchronisations
+(and a barrier plus max over ranks under torchrun).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--no-sweep] [--no-e2e] [--no-cpu]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("µs/call and effective HBM GB/s (% of GB300 peak) over the 12 "
+          "compress shapes")
+HEADLINE = (8, 131072, 128)
+L2_BYTES = 126 * 2 ** 20
+ROTATE_MIN_BYTES = 3 * L2_BYTES
+
+
+# ---- helpers shared with the multi-rank path (tested on CPU with gloo) -------
+
+def dist_env():
+    """(rank, world_size, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank compresses its own, independent batch of requests."""
+    return base_seed + 7919 * rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---- measured peaks, profiles, clocks ------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+KERNEL_SOURCES = ("kvc_compress.cu", "kvc_internal.h")
+
+
+def kernel_source_hash() -> str:
+    """Hash of the fused kernel's sources (ties ncu counters to a kernel)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kv_cache_compression_c128_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "kvc_compress_headline_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples (100 ms) around the timed region."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [(t, r) for t, r in self.samples if len(r) >= 10]
+        if self.uuid:
+            mine = [(t, r) for t, r in rows if self.uuid in r[1]]
+            rows = mine or rows
+        inside = [r for t, r in rows if self.t0 - 0.1 <= t <= self.t1 + 0.1]
+        if not inside and rows:  # timed region shorter than one sample period
+            mid = 0.5 * (self.t0 + self.t1)
+            inside = [min(rows, key=lambda tr: abs(tr[0] - mid))[1]]
+        if not inside:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[2]) for r in inside if num(r[2]) is not None]
+        reasons = set()
+        for r in inside:
+            for name, col in (("hw_slowdown", 6), ("hw_thermal_slowdown", 7),
+                              ("sw_thermal_slowdown", 8), ("sw_power_cap", 9)):
+                if r[col].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": num(inside[0][3]), "samples": len(inside),
+                "reasons": sorted(reasons),
+                "power_w_max": max((num(r[4]) or 0.0) for r in inside)}
+
+
+# ---- workload ------------------------------------------------------------------
+
+def _tensors(case, device, copies):
+    import torch
+
+    st_host = torch.from_numpy(case.state_bits.view(np.int16)).view(torch.bfloat16)
+    states = [st_host.to(device)]
+    for _ in range(copies - 1):
+        states.append(states[0].clone())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    d = dict(token_to_req=t(case.token_to_req), positions=t(case.positions),
+             boundary_token_indices=t(case.boundary_token_indices),
+             block_table=t(case.block_table), rms_norm_weight=t(case.rms_norm_weight),
+             cos_sin_cache=t(case.cos_sin_cache), kv_slot_mapping=t(case.kv_slot_mapping),
+             kv_cache=t(case.kv_cache))
+    return states, d
+
+
+def _copies_for(case) -> int:
+    b = case.state_bits.nbytes
+    return max(3, -(-ROTATE_MIN_BYTES // b))
+
+
+def time_device(kvc, case, device, steps: int, warmup: int, sampler=None,
+                graph_chunk: int = 250):
+    """Average seconds per call over `steps` graph-replayed launches."""
+    import torch
+
+    copies = _copies_for(case)
+    states, d = _tensors(case, device, copies)
+    stream = torch.cuda.Stream(device)
+    N = case.num_outputs
+    ws = torch.zeros(kvc.kvc_workspace_bytes(N), dtype=torch.uint8, device=device)
+
+    def call(i, s):
+        kvc.c128_256_512_compress(states[i % copies], block_size=case.block_size,
+                                  compress_ratio=case.compress_ratio,
+                                  rms_norm_eps=case.rms_norm_eps, stream=s, workspace=ws, **d)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, warmup)):
+            call(i, stream)
+    stream.synchronize()
+    assert kvc.kvc_get_device_error(stream.cuda_stream) == 0
+    # graphs of up to graph_chunk launches, rotating the state copies
+    chunk = max(1, min(graph_chunk, steps))
+    graphs = []
+    remaining = steps
+    pos = 0
+    while remaining > 0:
+        m = min(chunk, remaining)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(m):
+                call(pos + i, stream)
+        graphs.append(g)
+        pos += m
+        remaining -= m
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    # replay() launches on the current stream: make it the timed stream
+    with torch.cuda.stream(stream):
+        graphs[0].replay()                    # warm the graph path itself
+        torch.cuda.synchronize(device)
+        barrier()
+        if sampler:
+            sampler.mark(True)
+        ev0.record(stream)
+        for g in graphs:
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark(False)
+    barrier()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    assert kvc.kvc_get_device_error(stream.cuda_stream) == 0
+    del graphs
+    return elapsed / steps, elapsed
+
+
+def time_e2e(kvc, case, device, steps: int, warmup: int):
+    """Seconds per call through the public API from pinned host buffers:
+    H2D of every input, the call, D2H of kv_cache, all inside the region."""
+    import torch
+
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    host = dict(state_cache=pin(case.state_bits.view(np.int16)).view(torch.bfloat16),
+                token_to_req=pin(case.token_to_req), positions=pin(case.positions),
+                boundary_token_indices=pin(case.boundary_token_indices),
+                block_table=pin(case.block_table), rms_norm_weight=pin(case.rms_norm_weight),
+                cos_sin_cache=pin(case.cos_sin_cache), kv_slot_mapping=pin(case.kv_slot_mapping),
+                kv_cache=pin(case.kv_cache))
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    out = torch.empty_like(host["kv_cache"]).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size()
+    stream = torch.cuda.Stream(device)
+    ws = torch.zeros(kvc.kvc_workspace_bytes(case.num_outputs), dtype=torch.uint8, device=device)
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        kvc.c128_256_512_compress(block_size=case.block_size, compress_ratio=case.compress_ratio,
+                                  rms_norm_eps=case.rms_norm_eps, stream=stream, workspace=ws,
+                                  **dev)
+        out.copy_(dev["kv_cache"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            step()
+        stream.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        stream.synchronize()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    assert np.array_equal(out.numpy().shape, case.kv_cache.shape)
+    return elapsed / steps, h2d, d2h
+
+
+def time_oracle(case, max_outputs: int):
+    """Single-threaded oracle on the first `max_outputs` outputs of `case`."""
+    import oracle
+
+    oracle.build()
+    n = min(max_outputs, case.num_outputs)
+    kv = case.kv_cache.copy()
+    t0 = time.perf_counter()
+    res = oracle.compress(case.state_bits, case.token_to_req, case.positions,
+                          case.boundary_token_indices[:n], case.block_table,
+                          case.rms_norm_weight, case.cos_sin_cache, case.kv_slot_mapping, kv,
+                          case.block_size, case.compress_ratio, case.rms_norm_eps)
+    dt = time.perf_counter() - t0
+    assert res["status"] == 0
+    return dt, n
+
+
+def bytes_for(case, n_outputs=None) -> int:
+    n = case.num_outputs if n_outputs is None else n_outputs
+    c = case.compress_ratio
+    return n * c * 2048 + n * (c // case.block_size) * 4 + n * 28 + n * 256 + 2048 + n * 584
+
+
+# ---- main ------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    rank, world, local_rank = dist_env()
+    from kv_cache_compression_c128_gb300 import inputs
+
+    R, T, C = HEADLINE
+    workload = f"{R} reqs x {T // R} tokens, compress_ratio {C}, block_size 8 ({T // C} outputs)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, inputs, workload)
+        return
+
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(device)
+    import kv_cache_compression_c128_gb300 as kvc
+
+    kvc.build()
+    case = inputs.make_case(R, T, C, seed=rank_seed(inputs.BASE_SEED + inputs.BENCH_SHAPES.index(HEADLINE), rank),
+                            name="headline")
+    per_call_bytes = bytes_for(case)
+    props = torch.cuda.get_device_properties(device)
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(uuid.replace("GPU-", "") if uuid else None)
+    sampler.start()
+    time.sleep(0.3)
+    t_call, t_total = time_device(kvc, case, device, args.steps, args.warmup, sampler)
+    clocks = sampler.stop()
+    t_max = max_over_ranks(t_total, device if world > 1 else None)
+    ms_per_step = t_max / args.steps * 1e3
+    value = world * per_call_bytes * args.steps / t_max / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = per_call_bytes / t_call / 1e9
+    ctas, threads, smem = kvc.kvc_query_launch(case.num_outputs, C)
+
+    e2e = None
+    if not args.no_e2e:
+        e_steps = max(3, min(50, args.steps))
+        t_e2e, h2d, d2h = time_e2e(kvc, case, device, e_steps, 3)
+        t_e2e = max_over_ranks(t_e2e, device if world > 1 else None)
+        e2e = {"value": round(world * per_call_bytes / t_e2e / 1e9, 3), "unit": "GB/s",
+               "us_per_call": round(t_e2e * 1e6, 2), "steps": e_steps,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    sweep = None
+    if not args.no_sweep and rank == 0:
+        sweep = []
+        shapes = [(i, inputs.bench_case) for i in range(12)]
+        for i, make in shapes + [(c, None) for c in (128, 256, 512)]:
+            cs = inputs.bench_case(i) if make else inputs.ragged_case(i)
+            n_steps = 2000 if cs.state_bits.nbytes < 100 * 2 ** 20 else 600
+            tc, _ = time_device(kvc, cs, device, n_steps, 20)
+            b = bytes_for(cs)
+            sweep.append({"shape": cs.name, "outputs": cs.num_outputs, "bytes": b,
+                          "us_per_call": round(tc * 1e6, 3),
+                          "gb_s": round(b / tc / 1e9, 1),
+                          "pct_of_peak": round(100 * b / tc / 1e9 / peak, 1)})
+            del cs
+
+    cpu = None
+    if not args.no_cpu and rank == 0 and world >= 1:
+        n_sample = case.num_outputs
+        dt, n = time_oracle(case, n_sample)
+        cpu = {"value": round(bytes_for(case, n) / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"first {n} of the {case.num_outputs} outputs of the headline workload, "
+                         f"one pass, single-threaded C (float64 reduce), {dt:.2f} s"}
+
+    if rank != 0:
+        return
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "us_per_call": round(ms_per_step * 1e3, 3),
+        "pct_of_peak": round(100 * value / world / peak, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) bf16 state, random block permutation, "
+                "1+0.1N(0,1) weights, RoPE theta 10000, permuted slots",
+        "config": {"workload": workload, "num_reqs": R, "total_tokens": T,
+                   "compress_ratio": C, "block_size": 8, "outputs": case.num_outputs,
+                   "algorithmic_bytes_per_call": per_call_bytes,
+                   "l2": f"{_copies_for(case)} rotating state copies "
+                         f"({_copies_for(case) * case.state_bits.nbytes >> 20} MiB > L2)",
+                   "timing": "CUDA graphs of <=250 launches, CUDA events on the launching stream",
+                   "launch": {"ctas": ctas, "threads": threads, "smem_bytes": smem},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": traffic, "kernel": "kvc_compress_kernel",
+                     "algorithmic_bytes_per_launch": per_call_bytes},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "sweep": sweep,
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line))
+
+
+def run_reference(args, inputs, workload):
+    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    R, T, C = HEADLINE
+    case = inputs.make_case(R, T, C, seed=inputs.BASE_SEED + inputs.BENCH_SHAPES.index(HEADLINE),
+                            name="headline")
+    # size each step's sample so the whole run takes about a minute
+    dt1, n1 = time_oracle(case, 8)
+    per_output = dt1 / n1
+    n_sample = int(max(1, min(case.num_outputs, 60.0 / max(1, args.steps) / per_output)))
+    for _ in range(max(0, min(args.warmup, 1))):
+        time_oracle(case, n_sample)
+    tot = 0.0
+    n = 0
+    for _ in range(args.steps):
+        dt, n = time_oracle(case, n_sample)
+        tot += dt
+    per = tot / max(1, args.steps)
+    value = bytes_for(case, n) / per / 1e9
+    sample = (f"each step: first {n} of the {case.num_outputs} outputs of the headline "
+              f"workload, single-threaded C oracle (float64 reduce)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload, "num_reqs": R, "total_tokens": T,
+                       "compress_ratio": C, "block_size": 8},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -13,8 +13,10 @@ tolerance because the kernel reduces in fp32 where the oracle uses double):
    taken on the same fp32 input on both sides;
 3. against the oracle's own bytes: every byte outside the written slots is
    identical; per element the dequantised NOPE values differ by at most one
-   quantisation step, scale bytes by at most one, RoPE values by at most one
-   bf16 ulp.
+   quantisation step, scale bytes by at most one; RoPE values by at most one
+   bf16 ulp plus what the y tolerance allows after a norm-preserving
+   rotation: 2e-3 |(u, w)| + 1.5e-5 rms(y) (where u cos ~ w sin cancel, a
+   tiny difference in y is many ulps of the tiny result).
 """
 import numpy as np
 import pytest
@@ -71,7 +73,8 @@ def check_case(oracle_mod, case, flags=0, valid_outputs=None):
     assert np.array_equal(kv_g.reshape(-1)[~m], kv_o.reshape(-1)[~m])
     assert np.array_equal(kv_g.reshape(-1)[~m], case.kv_cache.reshape(-1)[~m])
     n_code_diff = 0
-    for s in slots:
+    y_rms = np.sqrt((res["y"].astype(np.float64) ** 2).mean(1))
+    for n, s in enumerate(slots):
         if s < 0:
             continue
         qg, eg, pg, rg = decode_slot(kv_g, s)
@@ -80,8 +83,11 @@ def check_case(oracle_mod, case, flags=0, valid_outputs=None):
         assert np.all(np.abs(eg - eo) <= 1)
         step = np.maximum(np.repeat(np.ldexp(1.0, eg), 64), np.repeat(np.ldexp(1.0, eo), 64))
         assert np.all(np.abs(dequant(qg, eg) - dequant(qo, eo)) <= step)
-        ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(ro), 1e-30))[1] - 8)
-        assert np.all(np.abs(rg - ro) <= ulp)
+        mag = np.maximum(np.abs(ro), np.abs(rg))
+        ulp = np.ldexp(1.0, np.frexp(np.maximum(mag, 1e-30))[1] - 8)
+        pair = np.repeat(np.hypot(res["y"][n, 448::2], res["y"][n, 449::2]), 2)
+        tol = ulp + Y_RTOL * pair + 1.5 * Y_ATOL_RMS * y_rms[n]
+        assert np.all(np.abs(rg.astype(np.float64) - ro) <= tol)
         n_code_diff += int(np.sum(qg != qo))
     # differing codes come only from y values within rounding of a code edge
     assert n_code_diff <= max(8, 2e-3 * 448 * max(1, case.num_outputs))
