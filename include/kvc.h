@@ -43,7 +43,9 @@ typedef enum {
                                a window that does not start on an 8-row block */
   KVC_ERR_CUDA = 3,         /* a CUDA runtime call failed */
   KVC_ERR_BAD_INDEX = 4,    /* (device) an index outside its array */
-  KVC_ERR_TIMEOUT = 5       /* (device) a pipeline wait ran past its limit */
+  KVC_ERR_TIMEOUT = 5,      /* (device) a pipeline wait ran past its limit */
+  KVC_ERR_SCRATCH_LIMIT = 6 /* kvc_compress_static: the problem needs more scratch
+                               than the library's built-in buffer holds */
 } kvc_status;
 
 /* flags: bits 0..15 force the number of CTAs of the launch (0 = automatic:
@@ -105,6 +107,44 @@ kvc_status kvc_compress(
     int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
     float* y_out, void* workspace, size_t workspace_bytes,
     uint32_t flags, void* stream);
+
+/*
+ * kvc_compress without a workspace argument, for callers that cannot
+ * allocate device memory: plugins that are handed only their input and
+ * output pointers, engines that reserve the whole device memory pool up front
+ * and forbid allocation at run time, and latency-critical paths that cannot
+ * afford cudaMalloc's implicit device synchronisation.  (The write-up has no
+ * counterpart; this is a property of this library's interface.)
+ *
+ * Scratch comes from an 8 MiB buffer inside the library (a file-scope
+ * __device__ array, held by every device that loads the library until the
+ * process exits).  Nothing is allocated: no cudaMalloc, no cudaFree, no
+ * allocating library routine.  The first call on a device looks up the
+ * buffer's device address (cudaGetSymbolAddress) and sets up the kernel for
+ * that device; make that first call before any stream capture on the device.
+ * Each call clears the buffer's arrival counters with cudaMemsetAsync on
+ * `stream`, then computes exactly what kvc_compress computes.
+ *
+ * Every call on a device shares the one buffer, which keeps the last call's
+ * contents: calls that overlap on the GPU (different streams, not ordered by
+ * events) race on it.  Order them.
+ *
+ * Limit: on a 152-SM GPU the buffer serves up to about one million outputs
+ * per call (kvc_workspace_bytes(num_outputs) must not exceed 8 MiB); larger
+ * problems return KVC_ERR_SCRATCH_LIMIT before anything is launched.
+ * Arguments, errors and flags are otherwise those of kvc_compress.
+ */
+kvc_status kvc_compress_static(
+    const void* state_cache, int64_t num_state_blocks,
+    const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
+    const int64_t* boundary_token_indices, int64_t num_outputs,
+    const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    const float* rms_norm_weight,
+    const float* cos_sin_cache, int64_t num_positions,
+    const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+    uint8_t* kv_cache, int64_t num_kv_pages,
+    int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
+    float* y_out, uint32_t flags, void* stream);
 
 /*
  * Launch shape kvc_compress would use for this problem on the current

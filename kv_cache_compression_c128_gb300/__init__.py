@@ -24,7 +24,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(_LIB_DIR, "libkvc.so")
-_SOURCES = ["kvc_compress.cu", "kvc_api.cu"]
+_SOURCES = ["kvc_compress.cu", "kvc_api.cu", "kvc_static.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 KVC_OK = 0
@@ -33,6 +33,7 @@ KVC_ERR_UNSUPPORTED = 2
 KVC_ERR_CUDA = 3
 KVC_ERR_BAD_INDEX = 4
 KVC_ERR_TIMEOUT = 5
+KVC_ERR_SCRATCH_LIMIT = 6
 KVC_FLAG_GRID_MASK = 0xFFFF
 
 HEAD_DIM = 512
@@ -116,6 +117,10 @@ def lib():
                 P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P, I64,
                 I32, I32, ctypes.c_float, P, P, ctypes.c_size_t, U32, P]
             L.kvc_compress.restype = ctypes.c_int
+            L.kvc_compress_static.argtypes = [
+                P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P, I64,
+                I32, I32, ctypes.c_float, P, U32, P]
+            L.kvc_compress_static.restype = ctypes.c_int
             L.kvc_query_launch.argtypes = [I64, I32, U32, P, P, P]
             L.kvc_query_launch.restype = ctypes.c_int
             L.kvc_get_device_error.argtypes = [P, P]
@@ -177,6 +182,24 @@ def kvc_compress(state_cache, num_state_blocks, token_to_req, positions, num_tok
         v(kv_slot_mapping), slot_mapping_len, v(kv_cache), num_kv_pages, block_size,
         compress_ratio, ctypes.c_float(rms_norm_eps), v(y_out), v(workspace),
         workspace_bytes, flags, v(stream)))
+
+
+def kvc_compress_static(state_cache, num_state_blocks, token_to_req, positions, num_tokens,
+                        boundary_token_indices, num_outputs, block_table, num_reqs,
+                        max_blocks_per_req, rms_norm_weight, cos_sin_cache, num_positions,
+                        kv_slot_mapping, slot_mapping_len, kv_cache, num_kv_pages, block_size,
+                        compress_ratio, rms_norm_eps, y_out, flags, stream) -> int:
+    """kvc_compress without a workspace, for callers that cannot allocate
+    device memory: the library's built-in 8 MiB scratch buffer is used
+    instead (shared by all calls on a device; order overlapping calls).
+    Raw integer pointers; returns the status."""
+    v = ctypes.c_void_p
+    return int(lib().kvc_compress_static(
+        v(state_cache), num_state_blocks, v(token_to_req), v(positions), num_tokens,
+        v(boundary_token_indices), num_outputs, v(block_table), num_reqs,
+        max_blocks_per_req, v(rms_norm_weight), v(cos_sin_cache), num_positions,
+        v(kv_slot_mapping), slot_mapping_len, v(kv_cache), num_kv_pages, block_size,
+        compress_ratio, ctypes.c_float(rms_norm_eps), v(y_out), flags, v(stream)))
 
 
 # ---- torch-facing wrapper with the statement's signature ----------------------

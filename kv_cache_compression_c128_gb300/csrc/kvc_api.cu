@@ -182,6 +182,8 @@ const char* kvc_error_string(kvc_status status) {
     case KVC_ERR_CUDA: return "CUDA runtime error";
     case KVC_ERR_BAD_INDEX: return "index outside its array";
     case KVC_ERR_TIMEOUT: return "pipeline wait timed out";
+    case KVC_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the library's built-in 8 MiB buffer holds";
   }
   return "unknown status";
 }
