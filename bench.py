@@ -82,7 +82,7 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = ("kvc_compress.cu", "kvc_internal.h")
+KERNEL_SOURCES = ("kvc_cluster.cu", "kvc_streamk.cu", "kvc_device.cuh", "kvc_internal.h")
 
 
 def kernel_source_hash() -> str:
@@ -380,7 +380,7 @@ def main():
     value = world * per_call_bytes * args.steps / t_max / 1e9
     peak, peak_kind = measured_peaks()
     achieved = per_call_bytes / t_call / 1e9
-    ctas, threads, smem = kvc.kvc_query_launch(case.num_outputs, C)
+    ctas, cluster, threads, smem = kvc.kvc_query_launch(case.num_outputs, C)
 
     e2e = None
     if not args.no_e2e:
@@ -432,7 +432,9 @@ def main():
                    "l2": f"{_copies_for(case)} rotating state copies "
                          f"({_copies_for(case) * case.state_bits.nbytes >> 20} MiB > L2)",
                    "timing": "CUDA graphs of <=250 launches, CUDA events on the launching stream",
-                   "launch": {"ctas": ctas, "threads": threads, "smem_bytes": smem},
+                   "launch": {"ctas": ctas, "cluster_size": cluster, "threads": threads,
+                              "smem_bytes": smem,
+                              "route": "cluster" if cluster else "stream-k"},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -48,9 +48,20 @@ typedef enum {
                                than the library's built-in buffer holds */
 } kvc_status;
 
-/* flags: bits 0..15 force the number of CTAs of the launch (0 = automatic:
- * one or two persistent CTAs per SM).  Other bits must be zero. */
+/*
+ * flags (0 = automatic choice of everything):
+ *   bits 0..15   force the launch size: clusters for the cluster route, CTAs
+ *                for the stream-K route (capped at what fits on the device);
+ *   bits 16..20  force the cluster size S (1, 2, 4, 8 or 16, at most C/8);
+ *   bit 24       use the stream-K route instead of the cluster route.
+ * The routes compute the same bytes (see kvc_query_launch); the flags exist
+ * for tuning and testing.  Other bits must be zero.
+ */
 #define KVC_FLAG_GRID_MASK 0xFFFFu
+#define KVC_FLAG_CLUSTER_SHIFT 16
+#define KVC_FLAG_CLUSTER_MASK (0x1Fu << KVC_FLAG_CLUSTER_SHIFT)
+#define KVC_FLAG_STREAM_K (1u << 24)
+#define KVC_FLAG_ALL (KVC_FLAG_GRID_MASK | KVC_FLAG_CLUSTER_MASK | KVC_FLAG_STREAM_K)
 
 /*
  * Bytes of device workspace kvc_compress needs for num_outputs outputs on
@@ -148,12 +159,14 @@ kvc_status kvc_compress_static(
 
 /*
  * Launch shape kvc_compress would use for this problem on the current
- * device: CTAs, threads per CTA and dynamic shared memory bytes.  Any out
- * pointer may be NULL.  flags as for kvc_compress.
+ * device: total CTAs, cluster size (0 for the stream-K route), threads per
+ * CTA and dynamic shared memory bytes per CTA.  Any out pointer may be NULL.
+ * flags as for kvc_compress; KVC_ERR_UNSUPPORTED if they ask for a cluster
+ * size the problem or the device cannot take.
  */
 kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio,
-                            uint32_t flags, int32_t* ctas, int32_t* threads,
-                            int32_t* smem_bytes);
+                            uint32_t flags, int32_t* ctas, int32_t* cluster_size,
+                            int32_t* threads, int32_t* smem_bytes);
 
 /*
  * Synchronises `stream`, then reads and clears the device error code

@@ -24,7 +24,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(_LIB_DIR, "libkvc.so")
-_SOURCES = ["kvc_compress.cu", "kvc_api.cu", "kvc_static.cu"]
+_SOURCES = ["kvc_cluster.cu", "kvc_streamk.cu", "kvc_api.cu", "kvc_static.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 KVC_OK = 0
@@ -35,6 +35,19 @@ KVC_ERR_BAD_INDEX = 4
 KVC_ERR_TIMEOUT = 5
 KVC_ERR_SCRATCH_LIMIT = 6
 KVC_FLAG_GRID_MASK = 0xFFFF
+KVC_FLAG_CLUSTER_SHIFT = 16
+KVC_FLAG_STREAM_K = 1 << 24
+
+
+def make_flags(route: str = "auto", count: int = 0, cluster_size: int = 0) -> int:
+    """kvc_compress flags: route 'auto' | 'cluster' | 'streamk', a forced
+    launch size (clusters or CTAs; 0 = automatic) and cluster size."""
+    f = int(count) & KVC_FLAG_GRID_MASK
+    if route == "streamk":
+        f |= KVC_FLAG_STREAM_K
+    else:
+        f |= (int(cluster_size) & 0x1F) << KVC_FLAG_CLUSTER_SHIFT
+    return f
 
 HEAD_DIM = 512
 KV_PAGE_BYTES = 64 * (576 + 8)
@@ -121,7 +134,7 @@ def lib():
                 P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P, I64,
                 I32, I32, ctypes.c_float, P, U32, P]
             L.kvc_compress_static.restype = ctypes.c_int
-            L.kvc_query_launch.argtypes = [I64, I32, U32, P, P, P]
+            L.kvc_query_launch.argtypes = [I64, I32, U32, P, P, P, P]
             L.kvc_query_launch.restype = ctypes.c_int
             L.kvc_get_device_error.argtypes = [P, P]
             L.kvc_get_device_error.restype = ctypes.c_int
@@ -148,13 +161,14 @@ def kvc_workspace_bytes(num_outputs: int) -> int:
 
 
 def kvc_query_launch(num_outputs: int, compress_ratio: int, flags: int = 0):
-    """(ctas, threads, dynamic smem bytes) of the launch for this problem."""
-    c, t, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    """(ctas, cluster size, threads, dynamic smem bytes) of the launch."""
+    c, k, t, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     st = lib().kvc_query_launch(int(num_outputs), int(compress_ratio), int(flags),
-                                ctypes.byref(c), ctypes.byref(t), ctypes.byref(s))
+                                ctypes.byref(c), ctypes.byref(k), ctypes.byref(t),
+                                ctypes.byref(s))
     if st != KVC_OK:
         raise KvcError(st, "kvc_query_launch")
-    return c.value, t.value, s.value
+    return c.value, k.value, t.value, s.value
 
 
 def kvc_get_device_error(stream: Optional[int] = None) -> int:

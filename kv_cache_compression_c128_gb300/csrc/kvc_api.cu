@@ -1,7 +1,7 @@
 // C ABI of the KV-cache window compressor (declared in include/kvc.h):
-// host-side argument validation, per-device launch capacity, workspace
-// sizing, device error reporting.  The computation itself is the fused
-// kernel of kvc_compress.cu.
+// host-side argument validation, per-device set-up, the choice between the
+// cluster route (kvc_cluster.cu) and the stream-K route (kvc_streamk.cu),
+// workspace sizing and device error reporting.
 
 #include <cuda_runtime.h>
 
@@ -14,19 +14,27 @@
 
 namespace {
 
+// Device error word: the first error code a kernel recorded since the last
+// kvc_get_device_error.  Kernels get its device address in Params::error.
+__device__ uint32_t g_error_word;
+
 constexpr int kMaxDevices = 64;
+constexpr int kClusterSizes[] = {1, 2, 4, 8, 16};
+constexpr int kNumClusterSizes = 5;
 
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  int ctas_per_sm = 0;
+  int streamk_ctas_per_sm = 0;
+  int cluster_cap[kNumClusterSizes] = {};  // co-resident clusters per size
   uint32_t* error_word = nullptr;
 };
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 
-// Per-device set-up on first use: shared-memory opt-in, occupancy, error word.
+// Per-device set-up on first use (with that device current): shared-memory
+// opt-in and occupancy of both routes, address of the error word.
 kvc_status device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_ERR_CUDA;
@@ -36,20 +44,22 @@ kvc_status device_info(DeviceInfo* out) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return KVC_ERR_CUDA;
-    const size_t smem = kvc::dynamic_smem_bytes();
-    if (cudaFuncSetAttribute(kvc::kernel_symbol(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = kvc::streamk_smem_bytes();
+    if (cudaFuncSetAttribute(kvc::streamk_kernel_symbol(),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return KVC_ERR_CUDA;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kvc::kernel_symbol(), kvc::kThreads,
-                                                      smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kvc::streamk_kernel_symbol(),
+                                                      kvc::kThreads, smem) != cudaSuccess ||
         per_sm < 1)
       return KVC_ERR_CUDA;
-    uint32_t* err = kvc::device_error_word();
-    if (err == nullptr) return KVC_ERR_CUDA;
+    for (int i = 0; i < kNumClusterSizes; ++i) d.cluster_cap[i] = kvc::cluster_capacity(kClusterSizes[i]);
+    void* err = nullptr;
+    if (cudaGetSymbolAddress(&err, g_error_word) != cudaSuccess || err == nullptr) return KVC_ERR_CUDA;
     d.sms = sms;
-    d.ctas_per_sm = per_sm;
-    d.error_word = err;
+    d.streamk_ctas_per_sm = per_sm;
+    d.error_word = static_cast<uint32_t*>(err);
     d.ready = true;
   }
   *out = d;
@@ -58,12 +68,73 @@ kvc_status device_info(DeviceInfo* out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int pick_ctas(const DeviceInfo& d, int64_t units, uint32_t flags) {
-  const int64_t cap = static_cast<int64_t>(d.sms) * d.ctas_per_sm;
-  int64_t g = (flags & KVC_FLAG_GRID_MASK) ? static_cast<int64_t>(flags & KVC_FLAG_GRID_MASK) : cap;
-  if (g > cap) g = cap;
-  if (g > units) g = units;
-  return static_cast<int>(g < 1 ? 1 : g);
+struct Route {
+  bool stream_k;
+  int count;     // stream-K: CTAs; cluster route: clusters
+  int cluster;   // cluster route: CTAs per output
+};
+
+int cluster_index(int S) {
+  for (int i = 0; i < kNumClusterSizes; ++i)
+    if (kClusterSizes[i] == S) return i;
+  return -1;
+}
+
+// Clusters for N outputs at a capacity of `cap` co-resident clusters: the
+// fewest that keep the largest per-cluster output count at its minimum, so
+// that every CTA streams (nearly) the same number of blocks.
+int64_t balanced_clusters(int64_t N, int cap) {
+  const int64_t most = N < cap ? N : cap;
+  const int64_t rounds = (N + most - 1) / most;
+  return (N + rounds - 1) / rounds;
+}
+
+// Cluster size for N outputs of K blocks: the estimated time of the slowest
+// CTA -- its blocks times the time one 16 KiB block takes when A CTAs share
+// the HBM (about 6.4 TB/s in all; one CTA's copy pipeline alone delivers
+// about 34 GB/s) -- plus about 1 us per cross-CTA merge.  Ties go to the
+// smaller cluster.  0 if no cluster size fits.
+int auto_cluster_size(const DeviceInfo& d, int64_t N, int64_t K) {
+  constexpr double kTotalBytesPerUs = 6.4e6, kCtaBytesPerUs = 3.4e4, kMergeUs = 1.0;
+  int best = 0;
+  double best_t = 1e300;
+  for (int i = 0; i < kNumClusterSizes; ++i) {
+    const int S = kClusterSizes[i];
+    if (S > K || d.cluster_cap[i] < 1) continue;
+    const int64_t ncl = balanced_clusters(N, d.cluster_cap[i]);
+    const double rounds = static_cast<double>((N + ncl - 1) / ncl);
+    const double kmax = static_cast<double>((K + S - 1) / S);
+    const double A = static_cast<double>(ncl) * S;
+    const double rate = kCtaBytesPerUs < kTotalBytesPerUs / A ? kCtaBytesPerUs : kTotalBytesPerUs / A;
+    const double t = rounds * kmax * kvc::kBlockBytes / rate + (S > 1 ? rounds * kMergeUs : 0.0);
+    if (t < best_t * (1.0 - 1e-9)) {
+      best_t = t;
+      best = S;
+    }
+  }
+  return best;
+}
+
+bool pick_route(const DeviceInfo& d, int64_t N, int64_t K, uint32_t flags, Route* r) {
+  const int forced_count = static_cast<int>(flags & KVC_FLAG_GRID_MASK);
+  const int forced_s = static_cast<int>((flags & KVC_FLAG_CLUSTER_MASK) >> KVC_FLAG_CLUSTER_SHIFT);
+  const int S = (flags & KVC_FLAG_STREAM_K) ? 0 : (forced_s ? forced_s : auto_cluster_size(d, N, K));
+  if (S == 0) {  // stream-K: asked for, or no cluster size fits this device
+    const int64_t units = N * K;
+    const int64_t cap = static_cast<int64_t>(d.sms) * d.streamk_ctas_per_sm;
+    int64_t g = forced_count ? forced_count : cap;
+    if (g > cap) g = cap;
+    if (g > units) g = units;
+    *r = Route{true, static_cast<int>(g < 1 ? 1 : g), 0};
+    return true;
+  }
+  const int ci = cluster_index(S);
+  if (ci < 0 || S > K || d.cluster_cap[ci] < 1) return false;
+  int64_t ncl = forced_count ? forced_count : balanced_clusters(N, d.cluster_cap[ci]);
+  if (ncl > d.cluster_cap[ci]) ncl = d.cluster_cap[ci];
+  if (ncl > N) ncl = N;
+  *r = Route{false, static_cast<int>(ncl < 1 ? 1 : ncl), S};
+  return true;
 }
 
 }  // namespace
@@ -73,21 +144,27 @@ extern "C" {
 size_t kvc_workspace_bytes(int64_t num_outputs) {
   DeviceInfo d;
   if (device_info(&d) != KVC_OK) return 0;
-  return kvc::workspace_layout(d.sms * d.ctas_per_sm, num_outputs).total;
+  return kvc::workspace_layout(d.sms * d.streamk_ctas_per_sm, num_outputs).total;
 }
 
 kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio, uint32_t flags,
-                            int32_t* ctas, int32_t* threads, int32_t* smem_bytes) {
+                            int32_t* ctas, int32_t* cluster_size, int32_t* threads,
+                            int32_t* smem_bytes) {
   if (num_outputs < 0 || compress_ratio <= 0 || compress_ratio % kvc::kBlockRows != 0 ||
-      (flags & ~KVC_FLAG_GRID_MASK) != 0)
+      (flags & ~KVC_FLAG_ALL) != 0)
     return KVC_ERR_INVALID_ARG;
   DeviceInfo d;
   const kvc_status st = device_info(&d);
   if (st != KVC_OK) return st;
-  const int64_t units = num_outputs * (compress_ratio / kvc::kBlockRows);
-  if (ctas) *ctas = units > 0 ? pick_ctas(d, units, flags) : 0;
-  if (threads) *threads = kvc::kThreads;
-  if (smem_bytes) *smem_bytes = static_cast<int32_t>(kvc::dynamic_smem_bytes());
+  Route r{false, 0, 1};
+  if (num_outputs > 0 && !pick_route(d, num_outputs, compress_ratio / kvc::kBlockRows, flags, &r))
+    return KVC_ERR_UNSUPPORTED;
+  if (ctas) *ctas = num_outputs > 0 ? (r.stream_k ? r.count : r.count * r.cluster) : 0;
+  if (cluster_size) *cluster_size = r.stream_k ? 0 : r.cluster;
+  if (threads) *threads = r.stream_k ? kvc::kThreads : kvc::cluster_threads();
+  if (smem_bytes)
+    *smem_bytes = static_cast<int32_t>(r.stream_k ? kvc::streamk_smem_bytes()
+                                                  : kvc::cluster_smem_bytes(r.cluster));
   return KVC_OK;
 }
 
@@ -101,7 +178,7 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
                         int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
                         float* y_out, void* workspace, size_t workspace_bytes, uint32_t flags,
                         void* stream) {
-  if (num_outputs < 0 || (flags & ~KVC_FLAG_GRID_MASK) != 0) return KVC_ERR_INVALID_ARG;
+  if (num_outputs < 0 || (flags & ~KVC_FLAG_ALL) != 0) return KVC_ERR_INVALID_ARG;
   if (block_size != kvc::kBlockRows) return KVC_ERR_UNSUPPORTED;
   if (compress_ratio <= 0 || compress_ratio % kvc::kBlockRows != 0) return KVC_ERR_UNSUPPORTED;
   if (!std::isfinite(rms_norm_eps) || rms_norm_eps < 0.f) return KVC_ERR_INVALID_ARG;
@@ -122,7 +199,7 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
   DeviceInfo d;
   const kvc_status st = device_info(&d);
   if (st != KVC_OK) return st;
-  const int max_ctas = d.sms * d.ctas_per_sm;
+  const int max_ctas = d.sms * d.streamk_ctas_per_sm;
   const kvc::WorkspaceLayout L = kvc::workspace_layout(max_ctas, num_outputs);
   if (workspace_bytes < L.total) return KVC_ERR_INVALID_ARG;
 
@@ -153,10 +230,15 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
   p.partials = reinterpret_cast<float*>(ws + L.partials);
   p.part_status = reinterpret_cast<int32_t*>(ws + L.status);
   p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
+  p.error = d.error_word;
 
-  const int ctas = pick_ctas(d, p.num_units, flags);
-  if (kvc::launch(p, ctas, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
-  return KVC_OK;
+  Route r;
+  if (!pick_route(d, num_outputs, p.blocks_per_output, flags, &r)) return KVC_ERR_UNSUPPORTED;
+  p.cluster_size = r.cluster;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      r.stream_k ? kvc::launch_streamk(p, r.count, s) : kvc::launch_cluster(p, r.count, s);
+  return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
 kvc_status kvc_get_device_error(void* stream, uint32_t* out_code) {
@@ -189,7 +271,8 @@ const char* kvc_error_string(kvc_status status) {
 }
 
 const char* kvc_version(void) {
-  return "kvc 0.1.0 sm_103a fused stream-K window compressor (bulk-copy ring, 6x16KiB stages)";
+  return "kvc 0.2.0 sm_103a: cluster route (S=1..16, bulk-copy ring 6x16KiB, st.async merges) "
+         "+ stream-K route";
 }
 
 }  // extern "C"

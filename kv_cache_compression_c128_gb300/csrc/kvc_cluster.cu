@@ -1,0 +1,433 @@
+// Cluster route of the KV-cache window compressor (sm_103a).
+//
+// Computes c128_256_512_compress of "From Attention to KV Cache Compression:
+// Notes from a KernelGen Optimization" (KernelGen Challenge 8 write-up): the
+// per-dimension softmax-weighted window sum of "How One Output Is Produced",
+// streamed as in "Online Softmax: Streaming Away the Window", then RMSNorm,
+// NOPE quantisation, RoPE and the packed slot store.
+//
+// Work decomposition.  Output n is handled by one thread-block cluster of S
+// CTAs (S = 1, 2, 4, 8, 16); rank j streams blocks [j K/S, (j+1) K/S) of the
+// window (K = C/8 blocks of 16 KiB).  Persistent clusters take contiguous,
+// equal ranges of outputs, so every CTA streams the same number of blocks.
+//
+// Inside a CTA (320 threads):
+//   warp 9  resolver: turns units into physical blocks (boundary index ->
+//           request/position/slot -> block_table) 32 at a time, two chunks
+//           ahead, into a shared-memory FIFO;
+//   warp 8  issuer: one cp.async.bulk of 16 KiB per unit into a kStages ring,
+//           each stage guarded by a full/empty mbarrier pair;
+//   warps 0-7 consumers: thread t owns dims 2t, 2t+1 and folds every staged
+//           block into its (max, denominator, numerator).
+// With S = 1 the consumers then finalise the output directly.  With S > 1
+// every rank pushes its partial state to the finaliser rank owning each dim
+// (F = min(S, 8) finalisers, 512/F dims each) with st.async, which completes
+// transaction bytes on that rank's mbarrier -- no fences, no remote polling.
+// Each finaliser merges the S partials from its own shared memory, pushes its
+// partial sum of squares to every rank the same way, and stores its slice of
+// the slot.  The sum-of-squares exchange also tells senders that their
+// previous partials were consumed, so a receive buffer is never overwritten
+// early.  Every wait is bounded; invalid indices are recorded, not trapped.
+
+#include <cuda_runtime.h>
+
+#include "kvc_device.cuh"
+
+namespace kvc {
+namespace {
+
+using namespace dev;
+
+constexpr int kClusterWarps = kConsumerWarps + 2;  // + issuer + resolver
+constexpr int kClusterThreads = kClusterWarps * 32;
+constexpr int kIssuerWarp = kConsumerWarps;
+constexpr int kResolverWarp = kConsumerWarps + 1;
+constexpr int kFifoChunk = 32;
+
+struct alignas(16) FifoEntry {
+  long long blk;    // physical block, -1 if unresolved
+  long long slot;   // output slot (first unit of an output only)
+  long long pc;     // compressed position (first unit of an output only)
+  int first;        // first unit of its output in this CTA
+  int piece;        // output index relative to the cluster's first output
+};
+
+template <int S>
+struct ClusterShared {
+  static constexpr int F = S < 8 ? S : 8;          // finaliser ranks
+  static constexpr int WD = kHeadDim / F;          // dims per finaliser
+  unsigned long long full_bar[kStages];
+  unsigned long long empty_bar[kStages];
+  unsigned long long fifo_full[2];
+  unsigned long long fifo_empty[2];
+  unsigned long long part_bar;                     // partials received
+  unsigned long long ss_bar;                       // partial sums received
+  FifoEntry fifo[2][kFifoChunk];
+  MetaRec meta[kMetaRing];
+  float recv[S > 1 ? S * 3 * WD : 1];              // [sender][m|den|num][WD]
+  float recv_bad[S > 1 ? S : 1];
+  float ss_recv[kMaxFinalizers];
+  FinalScratch fs;
+  uint32_t stage_ok[kStages];
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool aborted(const int* flag) {
+  return *reinterpret_cast<const volatile int*>(flag) != 0;
+}
+
+__device__ __forceinline__ void set_abort(int* flag) { *reinterpret_cast<volatile int*>(flag) = 1; }
+
+template <int S>
+__device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int64_t units, int k_lo,
+                         int kj) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t c = 0; c * kFifoChunk < units; ++c) {
+    const int64_t i = c * kFifoChunk + lane;
+    FifoEntry e{-1, -1, -1, 0, 0};
+    if (i < units) {
+      const int64_t q = i / kj;
+      const int kk = static_cast<int>(i - q * kj);
+      MetaRec rec;
+      resolve_unit(p, n0 + q, k_lo + kk, kk == 0, e.blk, rec);
+      e.slot = rec.slot;
+      e.pc = rec.pc;
+      e.first = (kk == 0);
+      e.piece = static_cast<int>(q);
+    }
+    const int h = static_cast<int>(c & 1);
+    const uint32_t ph = static_cast<uint32_t>((c >> 1) & 1);
+    bool ok = true;
+    if (lane == 0) {
+      ok = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.fifo_empty[h], ph ^ 1u);
+      if (!ok && !aborted(&sh.abort_flag)) {
+        record_error(p.error, kErrTimeout);
+        set_abort(&sh.abort_flag);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) return;
+    if (i < units) sh.fifo[h][lane] = e;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.fifo_full[h]);
+  }
+}
+
+template <int S>
+__device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int64_t units) {
+  if ((threadIdx.x & 31) != 0) return;
+  const uint64_t policy = evict_first_policy();
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued = 0, last_parity = 0;
+  bool stop = false;
+  for (int64_t c = 0; c * kFifoChunk < units && !stop; ++c) {
+    const int h = static_cast<int>(c & 1);
+    const uint32_t ph = static_cast<uint32_t>((c >> 1) & 1);
+    if (aborted(&sh.abort_flag) || !mbar_wait_bounded(&sh.fifo_full[h], ph)) {
+      if (!aborted(&sh.abort_flag)) {
+        record_error(p.error, kErrTimeout);
+        set_abort(&sh.abort_flag);
+      }
+      break;
+    }
+    const int64_t cnt = units - c * kFifoChunk < kFifoChunk ? units - c * kFifoChunk : kFifoChunk;
+    for (int j = 0; j < cnt; ++j) {
+      const FifoEntry e = sh.fifo[h][j];
+      if (aborted(&sh.abort_flag) || !mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u)) {
+        if (!aborted(&sh.abort_flag)) {
+          record_error(p.error, kErrTimeout);
+          set_abort(&sh.abort_flag);
+        }
+        stop = true;
+        break;
+      }
+      if (e.first) {
+        MetaRec& m = sh.meta[e.piece % kMetaRing];
+        m.slot = e.slot;
+        m.pc = e.pc;
+      }
+      if (e.blk >= 0) {
+        sh.stage_ok[stage] = 1;
+        mbar_arrive_expect_tx(&sh.full_bar[stage], kBlockBytes);
+        bulk_copy_g2s(ring + static_cast<size_t>(stage) * kBlockBytes,
+                      p.state + e.blk * (kBlockRows * kRowElems), kBlockBytes, &sh.full_bar[stage],
+                      policy);
+      } else {
+        sh.stage_ok[stage] = 0;
+        mbar_arrive(&sh.full_bar[stage]);
+      }
+      issued |= 1u << stage;
+      last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+    if (!stop) mbar_arrive(&sh.fifo_empty[h]);
+  }
+  // No bulk copy may still target this CTA's shared memory when it exits.
+  for (int s = 0; s < kStages; ++s)
+    if ((issued >> s) & 1u)
+      if (!mbar_wait_bounded(&sh.full_bar[s], (last_parity >> s) & 1u)) record_error(p.error, kErrTimeout);
+}
+
+template <int S>
+__device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* ring, int64_t n0,
+                          int64_t n1, int kj, uint32_t rank) {
+  using Sh = ClusterShared<S>;
+  constexpr int F = Sh::F, WD = Sh::WD;
+  const int t = threadIdx.x, lane = t & 31;
+  const bool finalizer = static_cast<int>(rank) < F;
+  const int dbase = finalizer ? static_cast<int>(rank) * WD : 0;
+  const bool active = finalizer && t < WD / 2;
+  const int d0 = dbase + 2 * t;
+  const bool rope = active && d0 >= kNopeDim;
+  const int jp = (d0 - kNopeDim) >> 1;
+  // where this thread's partial goes (S > 1): finaliser f, dim offset x
+  const int f = (2 * t) / WD, x = 2 * t - f * WD;
+  const uint32_t recv_l = smem_addr(sh.recv), bad_l = smem_addr(sh.recv_bad);
+  const uint32_t ss_l = smem_addr(sh.ss_recv);
+  const uint32_t part_bar_l = smem_addr(&sh.part_bar), ss_bar_l = smem_addr(&sh.ss_bar);
+  int stage = 0;
+  uint32_t phase = 0, mph = 0;
+  for (int64_t q = 0; q < n1 - n0; ++q) {
+    const int64_t n = n0 + q;
+    SoftmaxState s;
+    state_reset(s);
+    bool bad = false;
+    MetaRec meta{-1, -1};
+    float cs = 1.f, sn = 0.f;
+    for (int kk = 0; kk < kj; ++kk) {
+      bool ready = false;
+      if (!aborted(&sh.abort_flag)) {
+        ready = mbar_wait_bounded(&sh.full_bar[stage], phase);
+        if (!ready) {
+          record_error(p.error, kErrTimeout);
+          set_abort(&sh.abort_flag);
+        }
+      }
+      if (kk == 0 && ready) {
+        meta = sh.meta[q % kMetaRing];
+        if (rope && meta.pc >= 0) {
+          cs = __ldg(p.cos_sin + meta.pc * kRopeDim + jp);
+          sn = __ldg(p.cos_sin + meta.pc * kRopeDim + kRopeDim / 2 + jp);
+        }
+      }
+      if (ready && sh.stage_ok[stage]) {
+        fold_block(ring + static_cast<size_t>(stage) * kBlockBytes, t, s);
+      } else {
+        bad = true;
+      }
+      __syncwarp();
+      if (ready && lane == 0) mbar_arrive(&sh.empty_bar[stage]);
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+
+    if constexpr (S == 1) {
+      const float c0 = s.a0 / s.d0, c1 = s.a1 / s.d1;
+      const float total = consumer_sum_squares(sh.fs, c0, c1);
+      finalize_slice(p, sh.fs, n, true, 2 * t, c0, c1, bad, meta, cs, sn, total, 0, kHeadDim);
+    } else {
+      // push this rank's partial state to the finaliser of each dim
+      const uint32_t fbar = peer_addr(part_bar_l, f);
+      st_async_f2(peer_addr(recv_l + 4u * ((rank * 3 + 0) * WD + x), f), s.m0, s.m1, fbar);
+      st_async_f2(peer_addr(recv_l + 4u * ((rank * 3 + 1) * WD + x), f), s.d0, s.d1, fbar);
+      st_async_f2(peer_addr(recv_l + 4u * ((rank * 3 + 2) * WD + x), f), s.a0, s.a1, fbar);
+      const bool any_bad = consumer_any(bad);
+      if (t < F)
+        st_async_f32(peer_addr(bad_l + 4u * rank, t), any_bad ? 1.f : 0.f, peer_addr(part_bar_l, t));
+      float c0 = 0.f, c1 = 0.f;
+      bool mbad = any_bad;
+      if (finalizer) {
+        if (t == 0) mbar_arrive_expect_tx(&sh.part_bar, S * (WD * 12 + 4));
+        if (!mbar_wait_cluster_bounded(&sh.part_bar, mph)) {
+          record_error(p.error, kErrTimeout);
+          set_abort(&sh.abort_flag);
+          mbad = true;
+        }
+        if (active) {
+          float M0 = -INFINITY, M1 = -INFINITY, D0 = 0.f, D1 = 0.f, A0 = 0.f, A1 = 0.f;
+#pragma unroll
+          for (int j = 0; j < S; ++j) {
+            const float2 m = *reinterpret_cast<const float2*>(sh.recv + (j * 3 + 0) * WD + 2 * t);
+            const float2 d = *reinterpret_cast<const float2*>(sh.recv + (j * 3 + 1) * WD + 2 * t);
+            const float2 a = *reinterpret_cast<const float2*>(sh.recv + (j * 3 + 2) * WD + 2 * t);
+            const float nm0 = fmaxf(M0, m.x), nm1 = fmaxf(M1, m.y);
+            const float r0 = fast_ex2((M0 - nm0) * kLog2e), r1 = fast_ex2((M1 - nm1) * kLog2e);
+            const float f0 = fast_ex2((m.x - nm0) * kLog2e), f1 = fast_ex2((m.y - nm1) * kLog2e);
+            D0 = fmaf(d.x, f0, D0 * r0);
+            D1 = fmaf(d.y, f1, D1 * r1);
+            A0 = fmaf(a.x, f0, A0 * r0);
+            A1 = fmaf(a.y, f1, A1 * r1);
+            M0 = nm0;
+            M1 = nm1;
+            mbad |= sh.recv_bad[j] != 0.f;
+          }
+          c0 = A0 / D0;
+          c1 = A1 / D1;
+        }
+        // this slice's sum of squares, pushed to every rank
+        const float ssw = warp_sum(active ? c0 * c0 + c1 * c1 : 0.f);
+        if (lane == 0) sh.fs.red[t >> 5] = ssw;
+        consumer_sync();
+        if (t == 0) {
+          float mine = 0.f;
+#pragma unroll
+          for (int i = 0; i < kConsumerWarps; ++i) mine += sh.fs.red[i];
+#pragma unroll
+          for (int r = 0; r < S; ++r) st_async_f32(peer_addr(ss_l + 4u * rank, r), mine, peer_addr(ss_bar_l, r));
+        }
+      }
+      if (t == 0) mbar_arrive_expect_tx(&sh.ss_bar, F * 4);
+      if (!mbar_wait_cluster_bounded(&sh.ss_bar, mph)) {
+        record_error(p.error, kErrTimeout);
+        set_abort(&sh.abort_flag);
+        mbad = true;
+      }
+      mph ^= 1u;
+      if (finalizer) {
+        float total = 0.f;
+#pragma unroll
+        for (int i = 0; i < F; ++i) total += sh.ss_recv[i];
+        finalize_slice(p, sh.fs, n, active, d0, c0, c1, mbad, meta, cs, sn, total, dbase, WD);
+      } else {
+        consumer_sync();  // sh.fs.red is rewritten by the next output
+      }
+    }
+  }
+}
+
+template <int S>
+__global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  ClusterShared<S>& sh =
+      *reinterpret_cast<ClusterShared<S>*>(smem + static_cast<size_t>(kStages) * kBlockBytes);
+  const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
+  const int64_t c = blockIdx.x / S, ncl = gridDim.x / S;
+  const int64_t N = p.num_outputs;
+  const int64_t n0 = c * N / ncl, n1 = (c + 1) * N / ncl;
+  const int K = p.blocks_per_output;
+  const int k_lo = static_cast<int>(rank) * K / S;
+  const int kj = (static_cast<int>(rank) + 1) * K / S - k_lo;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh.full_bar[s], 1);
+      mbar_init(&sh.empty_bar[s], kConsumerWarps);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sh.fifo_full[h], 1);
+      mbar_init(&sh.fifo_empty[h], 1);
+    }
+    mbar_init(&sh.part_bar, 1);
+    mbar_init(&sh.ss_bar, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  // Wait for the previous grid on the stream (programmatic dependent launch)
+  // before touching any global memory, and let the next one start launching.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (S > 1) {
+    cluster_sync_all();  // every rank's barriers exist before any remote store
+  } else {
+    __syncthreads();
+  }
+  if (n0 < n1 && kj > 0) {
+    const int warp = threadIdx.x >> 5;
+    const int64_t units = (n1 - n0) * kj;
+    if (warp == kResolverWarp) {
+      resolver<S>(p, sh, n0, units, k_lo, kj);
+    } else if (warp == kIssuerWarp) {
+      issuer<S>(p, sh, smem, units);
+    } else {
+      consumers<S>(p, sh, smem, n0, n1, kj, rank);
+    }
+  }
+  if (S > 1) cluster_sync_all();  // no CTA leaves while a peer may still write to it
+}
+
+template <int S>
+size_t smem_bytes_of() {
+  return static_cast<size_t>(kStages) * kBlockBytes + sizeof(ClusterShared<S>);
+}
+
+template <int S>
+cudaLaunchConfig_t config_of(int clusters, cudaStream_t stream, cudaLaunchAttribute* attrs) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * S));
+  cfg.blockDim = dim3(kClusterThreads);
+  cfg.dynamicSmemBytes = smem_bytes_of<S>();
+  cfg.stream = stream;
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+template <int S>
+int prepare_and_capacity() {
+  const void* fn = reinterpret_cast<const void*>(&kvc_cluster_kernel<S>);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes_of<S>())) != cudaSuccess)
+    return 0;
+  if (S > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return 0;
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = config_of<S>(1, nullptr, attrs);
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, &kvc_cluster_kernel<S>, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int S>
+cudaError_t launch_of(const Params& p, int clusters, cudaStream_t stream) {
+  cudaLaunchAttribute attrs[2];
+  cudaLaunchConfig_t cfg = config_of<S>(clusters, stream, attrs);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+int cluster_threads() { return kClusterThreads; }
+
+size_t cluster_smem_bytes(int S) {
+  switch (S) {
+    case 1: return smem_bytes_of<1>();
+    case 2: return smem_bytes_of<2>();
+    case 4: return smem_bytes_of<4>();
+    case 8: return smem_bytes_of<8>();
+    case 16: return smem_bytes_of<16>();
+  }
+  return 0;
+}
+
+int cluster_capacity(int S) {
+  int n = 0;
+  switch (S) {
+    case 1: n = prepare_and_capacity<1>(); break;
+    case 2: n = prepare_and_capacity<2>(); break;
+    case 4: n = prepare_and_capacity<4>(); break;
+    case 8: n = prepare_and_capacity<8>(); break;
+    case 16: n = prepare_and_capacity<16>(); break;
+  }
+  (void)cudaGetLastError();  // a refused size leaves no sticky error behind
+  return n;
+}
+
+cudaError_t launch_cluster(const Params& p, int clusters, cudaStream_t stream) {
+  switch (p.cluster_size) {
+    case 1: return launch_of<1>(p, clusters, stream);
+    case 2: return launch_of<2>(p, clusters, stream);
+    case 4: return launch_of<4>(p, clusters, stream);
+    case 8: return launch_of<8>(p, clusters, stream);
+    case 16: return launch_of<16>(p, clusters, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvc

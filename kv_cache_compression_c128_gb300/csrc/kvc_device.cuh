@@ -1,0 +1,425 @@
+// Device-side building blocks shared by the two kernels of the KV-cache
+// window compressor (kvc_streamk.cu, kvc_cluster.cu): PTX wrappers for
+// mbarriers, bulk copies and cluster shared memory, the per-dimension online
+// softmax fold, block-table resolution, and the finaliser (RMSNorm, NOPE
+// quantisation, RoPE, slot store) of "How One Output Is Produced" in the
+// KernelGen Challenge 8 write-up, with the byte rules of its section "The
+// Finalizer's Sharp Edges".
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace dev {
+
+constexpr uint32_t kErrUnsupported = 2;
+constexpr uint32_t kErrBadIndex = 4;
+constexpr uint32_t kErrTimeout = 5;
+constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Slot record of one output piece, handed from the copy-issuing warp to the
+// consumer warps through shared memory.
+struct alignas(16) MetaRec {
+  long long slot;  // destination slot (< 0: do not write)
+  long long pc;    // compressed position (< 0: invalid output)
+};
+
+// ---- PTX wrappers -------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase of `bar` with the given parity; false after the limit.
+static __device__ __noinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
+// As mbar_wait_bounded, with cluster-scope acquire: for barriers completed by
+// other CTAs of the cluster (remote stores with complete_tx).
+__device__ __forceinline__ bool mbar_try_wait_cluster(unsigned long long* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_cluster_bounded(unsigned long long* bar,
+                                                              uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// One bulk (1-D) copy global -> shared, completing on `bar` as tx bytes.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              unsigned long long* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Named barrier 1 over the 256 consumer threads (the other warps never join).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// OR of `v` over the consumer threads (also a consumer barrier).
+__device__ __forceinline__ bool consumer_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kConsumerThreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void record_error(uint32_t* err, uint32_t code) { atomicCAS(err, 0u, code); }
+
+// ---- cluster shared memory ----------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Shared-memory address of `local` (this CTA) in the CTA of cluster rank r.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t r) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(r));
+  return a;
+}
+
+// Remote stores into another CTA's shared memory that complete `bytes` of
+// transaction count on that CTA's mbarrier once the data is visible there.
+__device__ __forceinline__ void st_async_f2(uint32_t remote, float x, float y, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(remote),
+      "f"(x), "f"(y), "r"(remote_bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t remote, float x, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote),
+               "f"(x), "r"(remote_bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// ---- bf16 and float helpers -----------------------------------------------------
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ceil(log2(a / 127)) for a finite, normal a > 0, exactly: with a = m 2^E,
+// m in [1, 2), 127 * 2^e >= a  <=>  e >= E + log2(m / 127), and
+// log2(m / 127) lies in (-7, -5]; it exceeds -6 exactly when m > 127/64,
+// i.e. when the 23-bit mantissa field exceeds 0x7E0000.
+__device__ __forceinline__ int scale_exponent(float a) {
+  const uint32_t bits = __float_as_uint(a);
+  const int e_a = static_cast<int>(bits >> 23) - 127;
+  return e_a - 6 + ((bits & 0x7FFFFFu) > 0x7E0000u ? 1 : 0);
+}
+
+__device__ __forceinline__ uint32_t bf16_bits_rn(float x) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+// ---- online softmax over the window -----------------------------------------------
+
+struct SoftmaxState {
+  float m0, m1, d0, d1, a0, a1;  // running max, denominator, numerator (2 dims)
+};
+
+__device__ __forceinline__ void state_reset(SoftmaxState& s) {
+  s.m0 = s.m1 = -INFINITY;
+  s.d0 = s.d1 = s.a0 = s.a1 = 0.f;
+}
+
+// Fold one staged 8-row block (8 rows x [512 values | 512 scores] bf16) into
+// thread t's dimensions 2t, 2t+1: the block's score maximum (bf16x2, exact)
+// rescales the running state once, then every row adds exp(s - m) to the
+// denominator and exp(s - m) * v to the numerator (packed f32x2 arithmetic;
+// exp as ex2 of a log2e-scaled argument).
+__device__ __forceinline__ void fold_block(const uint8_t* blk, int t, SoftmaxState& s) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(blk);
+  uint32_t sw[kBlockRows], vw[kBlockRows];
+#pragma unroll
+  for (int r = 0; r < kBlockRows; ++r) {
+    sw[r] = w[r * (kRowElems / 2) + (kHeadDim / 2) + t];
+    vw[r] = w[r * (kRowElems / 2) + t];
+  }
+  const uint32_t mx = bf16x2_max(bf16x2_max(bf16x2_max(sw[0], sw[1]), bf16x2_max(sw[2], sw[3])),
+                                 bf16x2_max(bf16x2_max(sw[4], sw[5]), bf16x2_max(sw[6], sw[7])));
+  const float nm0 = fmaxf(s.m0, bf16_lo(mx));
+  const float nm1 = fmaxf(s.m1, bf16_hi(mx));
+  const float r0 = fast_ex2((s.m0 - nm0) * kLog2e);  // 0 on the first block
+  const float r1 = fast_ex2((s.m1 - nm1) * kLog2e);
+  const unsigned long long l2 = pack2(kLog2e, kLog2e);
+  const unsigned long long negmb = pack2(-nm0 * kLog2e, -nm1 * kLog2e);
+  unsigned long long dd = 0ull, aa = 0ull;
+#pragma unroll
+  for (int r = 0; r < kBlockRows; ++r) {
+    float x0, x1;
+    unpack2(fma2(pack2(bf16_lo(sw[r]), bf16_hi(sw[r])), l2, negmb), x0, x1);
+    const unsigned long long e = pack2(fast_ex2(x0), fast_ex2(x1));
+    dd = add2(dd, e);
+    aa = fma2(e, pack2(bf16_lo(vw[r]), bf16_hi(vw[r])), aa);
+  }
+  float d0, d1, a0, a1;
+  unpack2(dd, d0, d1);
+  unpack2(aa, a0, a1);
+  s.d0 = fmaf(s.d0, r0, d0);
+  s.d1 = fmaf(s.d1, r1, d1);
+  s.a0 = fmaf(s.a0, r0, a0);
+  s.a1 = fmaf(s.a1, r1, a1);
+  s.m0 = nm0;
+  s.m1 = nm1;
+}
+
+// ---- block table resolution -------------------------------------------------------
+
+// Physical block of unit (n, k) of the window (blk = -1, error recorded, if
+// any index is bad) and, when want_meta, the output's slot and compressed
+// position pc = floor(p / C) * C.  The slot is loaded together with the
+// request and position, so the chain before the first bulk copy is three
+// dependent loads deep.
+__device__ __forceinline__ void resolve_unit(const Params& p, int64_t n, int k, bool want_meta,
+                                             long long& blk, MetaRec& rec) {
+  blk = -1;
+  rec = MetaRec{-1, -1};
+  const int64_t b = __ldg(p.bti + n);
+  if (b < 0 || b >= p.num_tokens) { record_error(p.error, kErrBadIndex); return; }
+  const int64_t r = __ldg(p.token_to_req + b);
+  const int64_t pos = __ldg(p.positions + b);
+  const int64_t slot = want_meta ? __ldg(p.slot_map + (p.slot_by_token ? b : n)) : -1;
+  const int64_t t0 = pos - p.compress_ratio + 1;
+  if (r < 0 || r >= p.num_reqs || t0 < 0) { record_error(p.error, kErrBadIndex); return; }
+  if (t0 & (kBlockRows - 1)) { record_error(p.error, kErrUnsupported); return; }
+  const int64_t l = t0 / kBlockRows + k;
+  if (l >= p.max_blocks) { record_error(p.error, kErrBadIndex); return; }
+  const int64_t g = __ldg(p.block_table + r * p.max_blocks + l);
+  if (g < 0 || g >= p.num_blocks) { record_error(p.error, kErrBadIndex); return; }
+  blk = g;
+  if (want_meta) {
+    const int64_t pc = (pos / p.compress_ratio) * p.compress_ratio;
+    if (pc >= p.num_positions) { record_error(p.error, kErrBadIndex); blk = -1; return; }
+    if (slot >= 0 && (slot / kSlotsPerPage) >= p.num_pages) {
+      record_error(p.error, kErrBadIndex);
+      blk = -1;
+      return;
+    }
+    rec.slot = slot;
+    rec.pc = pc;
+  }
+}
+
+// ---- finaliser ------------------------------------------------------------------------
+
+// Shared-memory scratch of the finaliser (one per CTA).
+struct FinalScratch {
+  alignas(16) uint8_t pack[kTokenStride + kScaleDim];  // the slot's 584 bytes
+  float red[kConsumerWarps];
+};
+
+// Sum of c0^2 + c1^2 over the 256 consumer threads (each owning 2 dims).
+__device__ __forceinline__ float consumer_sum_squares(FinalScratch& fs, float c0, float c1) {
+  const int t = threadIdx.x;
+  const float ss = warp_sum(c0 * c0 + c1 * c1);
+  if ((t & 31) == 0) fs.red[t >> 5] = ss;
+  consumer_sync();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kConsumerWarps; ++i) tot += fs.red[i];
+  return tot;
+}
+
+// RMSNorm, NOPE quantisation, RoPE and the store of dims [dbase, dbase + wd)
+// of output n.  Thread t < wd/2 is `active` and owns dims d0 = dbase + 2t and
+// d0 + 1 with window sums c0, c1; `total` is the sum of c^2 over all 512
+// dims.  wd is a multiple of 64, so every 64-dim quantisation group lies in
+// one warp and the RoPE dims 448..511 in the last.  The slice's bytes are
+// [dbase, dbase + wd) of the payload (up to 576 for the slice holding the
+// RoPE dims) and scale bytes [dbase/64, (dbase + wd)/64) (the last one is
+// the zero padding byte).  All 256 consumer threads call this (it holds
+// consumer barriers).
+__device__ __forceinline__ void finalize_slice(const Params& p, FinalScratch& fs, int64_t n,
+                                               bool active, int d0, float c0, float c1, bool bad,
+                                               const MetaRec& meta, float cs, float sn, float total,
+                                               int dbase, int wd) {
+  const int t = threadIdx.x, lane = t & 31;
+  const bool invalid = consumer_any(bad) || meta.pc < 0;
+  const float rho = __frsqrt_rn(total * (1.0f / kHeadDim) + p.eps);
+  if (active) {
+    const float2 w = __ldg(reinterpret_cast<const float2*>(p.weight + d0));
+    const float y0 = __fmul_rn(__fmul_rn(c0, rho), w.x);
+    const float y1 = __fmul_rn(__fmul_rn(c1, rho), w.y);
+    if (p.y_out != nullptr && !invalid)
+      *reinterpret_cast<float2*>(p.y_out + n * kHeadDim + d0) = make_float2(y0, y1);
+    if (d0 < kNopeDim) {
+      // bf16 round trip, group amax (one warp = one 64-dim group), exponent,
+      // truncating codes, two's-complement bytes
+      const float z0 = __bfloat162float(__float2bfloat16_rn(y0));
+      const float z1 = __bfloat162float(__float2bfloat16_rn(y1));
+      const float a = fmaxf(warp_max(fmaxf(fabsf(z0), fabsf(z1))), 1.0e-4f);
+      const int e = scale_exponent(a);
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+      int q0 = __float2int_rz(__fmul_rn(z0, inv));
+      int q1 = __float2int_rz(__fmul_rn(z1, inv));
+      q0 = max(-127, min(127, q0));
+      q1 = max(-127, min(127, q1));
+      *reinterpret_cast<uint16_t*>(fs.pack + d0) =
+          static_cast<uint16_t>((q0 & 0xFF) | ((q1 & 0xFF) << 8));
+      if (lane == 0) fs.pack[kTokenStride + d0 / kGroup] = static_cast<uint8_t>(e + 127);
+    } else {
+      // GPT-J pair j on dims (448 + 2j, 449 + 2j), one rounding per operation
+      const int j = (d0 - kNopeDim) >> 1;
+      const float ru = __fsub_rn(__fmul_rn(y0, cs), __fmul_rn(y1, sn));
+      const float rw = __fadd_rn(__fmul_rn(y1, cs), __fmul_rn(y0, sn));
+      *reinterpret_cast<uint32_t*>(fs.pack + kNopeDim + 4 * j) =
+          bf16_bits_rn(ru) | (bf16_bits_rn(rw) << 16);
+      if (j == 0) fs.pack[kTokenStride + kScaleDim - 1] = 0;
+    }
+  }
+  consumer_sync();
+  if (!invalid && meta.slot >= 0) {
+    uint8_t* page = p.kv + (meta.slot / kSlotsPerPage) * kPageBytes;
+    const int64_t off = meta.slot % kSlotsPerPage;
+    const int pb0 = dbase;
+    const int pb1 = (dbase + wd == kHeadDim) ? kTokenStride : dbase + wd;
+    const int chunks = (pb1 - pb0) / 16;
+    const int sb0 = dbase / kGroup, sb1 = (dbase + wd) / kGroup;
+    if (t < chunks) {
+      reinterpret_cast<uint4*>(page + off * kTokenStride + pb0)[t] =
+          reinterpret_cast<const uint4*>(fs.pack + pb0)[t];
+    } else if (t < chunks + (sb1 - sb0)) {
+      if (sb1 - sb0 == kScaleDim) {  // whole scale record: one 8-byte store
+        if (t == chunks)
+          *reinterpret_cast<uint2*>(page + kScaleBase + off * kScaleDim) =
+              *reinterpret_cast<const uint2*>(fs.pack + kTokenStride);
+      } else {
+        const int i = sb0 + (t - chunks);
+        page[kScaleBase + off * kScaleDim + i] = fs.pack[kTokenStride + i];
+      }
+    }
+  }
+  consumer_sync();  // fs is reused by the next output
+}
+
+}  // namespace dev
+}  // namespace kvc

@@ -1,5 +1,5 @@
-// Internal interface between the C ABI layer (kvc_api.cu) and the fused
-// kernel (kvc_compress.cu).  Not installed; not part of the ABI.
+// Internal interface between the C ABI layer (kvc_api.cu) and the two
+// kernel routes (kvc_cluster.cu, kvc_streamk.cu).  Not part of the ABI.
 #pragma once
 
 #include <cstddef>
@@ -25,10 +25,13 @@ constexpr int kScaleDim = 8;
 constexpr int64_t kPageBytes = kSlotsPerPage * (kTokenStride + kScaleDim);
 constexpr int kScaleBase = kSlotsPerPage * kTokenStride;   // 36864
 
-// CTA shape: 8 consumer warps (thread t owns dims 2t, 2t+1) + 1 producer warp.
+// CTA shape: 8 consumer warps (thread t owns dims 2t, 2t+1) + 1 producer
+// warp (stream-K route; the cluster route adds a resolver warp).
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kMaxClusterSize = 16;
+constexpr int kMaxFinalizers = 8;
 constexpr int kStages = 6;                                 // 16 KiB ring stages
 constexpr int kMetaRing = kStages + 2;                     // per-output records
 
@@ -58,10 +61,11 @@ struct Params {
   int blocks_per_output;          // K = C / 8
   int64_t num_units;              // U = N * K: one unit = one 8-row block
   float eps;
+  int cluster_size;               // cluster route: CTAs per output (S)
   float* partials;                // [2 * max_ctas][kPartialFloats]
   int32_t* part_status;           // [2 * max_ctas]
   int32_t* counters;              // [num_outputs]
-  uint32_t* error;                // device error word
+  uint32_t* error;                // device error word (first error code wins)
 };
 
 // Workspace layout (byte offsets), given the device's CTA capacity.
@@ -70,9 +74,15 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(int max_ctas, int64_t num_outputs);
 
-size_t dynamic_smem_bytes();
-const void* kernel_symbol();
-uint32_t* device_error_word();     // device address of the error word (per device)
-cudaError_t launch(const Params& p, int ctas, cudaStream_t stream);
+// stream-K route (kvc_streamk.cu)
+size_t streamk_smem_bytes();
+const void* streamk_kernel_symbol();
+cudaError_t launch_streamk(const Params& p, int ctas, cudaStream_t stream);
+
+// cluster route (kvc_cluster.cu); cluster sizes 1, 2, 4, 8, 16
+int cluster_threads();
+size_t cluster_smem_bytes(int cluster_size);
+int cluster_capacity(int cluster_size);  // sets the kernel up; co-resident clusters (0: refused)
+cudaError_t launch_cluster(const Params& p, int clusters, cudaStream_t stream);
 
 }  // namespace kvc

@@ -76,7 +76,7 @@ _GOOD = dict(state_cache=0x10000, num_state_blocks=1024, token_to_req=0x20000,
     (dict(compress_ratio=100), 2),
     (dict(compress_ratio=0), 2),
     (dict(num_outputs=-1), 1),
-    (dict(flags=1 << 20), 1),
+    (dict(flags=1 << 28), 1),
     (dict(rms_norm_eps=float("nan")), 1),
     (dict(rms_norm_eps=-1.0), 1),
     (dict(state_cache=0), 1),
@@ -103,6 +103,14 @@ def test_query_launch_rejects_bad_arguments(kvc):
         kvc.kvc_query_launch(64, 100)
     with pytest.raises(kvc.KvcError):
         kvc.kvc_query_launch(-1, 128)
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_query_launch(64, 128, 1 << 28)
+
+
+def test_make_flags(kvc):
+    assert kvc.make_flags() == 0
+    assert kvc.make_flags("cluster", 3, 8) == 3 | (8 << 16)
+    assert kvc.make_flags("streamk", 13) == 13 | (1 << 24)
 
 
 def test_torch_wrapper_rejects_cpu_tensors(kvc):

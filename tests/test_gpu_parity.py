@@ -98,11 +98,28 @@ SMALL = [(1, 256, 8), (2, 1024, 16), (2, 2048, 128), (1, 4096, 512), (3, 3072, 6
          (4, 4096, 256)]
 
 
+ROUTES = ([("auto", 0, 0)] + [("streamk", g, 0) for g in (1, 3, 7, 13, 64)]
+          + [("cluster", n, S) for S in (1, 2, 4, 8, 16) for n in (0, 1, 3)])
+
+
 @pytest.mark.parametrize("R,T,C", SMALL)
-@pytest.mark.parametrize("grid", [0, 1, 3, 7, 13, 64])
-def test_small_cases_all_grid_splits(kvc, oracle_mod, R, T, C, grid):
+@pytest.mark.parametrize("route,count,S", ROUTES)
+def test_small_cases_every_route(kvc, oracle_mod, R, T, C, route, count, S):
+    if S > C // 8:
+        pytest.skip("cluster larger than the window's block count")
     case = inputs.make_case(R, T, C, seed=inputs.BASE_SEED + 500 + C + R, kv_fill=11)
-    check_case(oracle_mod, case, flags=grid)
+    check_case(oracle_mod, case, flags=kvc.make_flags(route, count, S))
+
+
+@pytest.mark.parametrize("C", [128, 512])
+@pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
+def test_full_size_every_cluster_size(kvc, oracle_mod, C, S):
+    case = inputs.make_case(4, 32768, C, seed=inputs.BASE_SEED + 600 + C, kv_fill=12)
+    check_case(oracle_mod, case, flags=kvc.make_flags("cluster", 0, S))
+
+
+def test_full_size_stream_k_route(kvc, oracle_mod):
+    check_case(oracle_mod, inputs.bench_case(3), flags=kvc.make_flags("streamk"))
 
 
 @pytest.mark.parametrize("case_id", range(12))
@@ -121,7 +138,9 @@ def test_ragged_with_odd_grids(kvc, oracle_mod):
     L = inputs.ragged_lengths(5, 20480, 128, seed=77)
     case = inputs.make_case(5, 20480, 128, seed=78, lengths=L, kv_fill=79)
     for grid in (1, 5, 17, 151, 299):
-        check_case(oracle_mod, case, flags=grid)
+        check_case(oracle_mod, case, flags=kvc.make_flags("streamk", grid))
+    for n, S in ((1, 2), (5, 4), (17, 8), (7, 16), (151, 1)):
+        check_case(oracle_mod, case, flags=kvc.make_flags("cluster", n, S))
 
 
 def test_deterministic_repeat(kvc, oracle_mod):
@@ -177,7 +196,7 @@ def _expect_device_error(kvc, case, code, bad_outputs, oracle_mod, grid=0):
     return kv_g
 
 
-@pytest.mark.parametrize("grid", [0, 3])
+@pytest.mark.parametrize("grid", [0, 3 | (1 << 24), 2 << 16, 8 << 16])
 def test_bad_block_index_is_reported_and_skipped(kvc, oracle_mod, grid):
     case = inputs.make_case(2, 2048, 128, seed=85, kv_fill=86)
     case.block_table = case.block_table.copy()

@@ -47,9 +47,11 @@ def _raw_args(d, case, y, stream):
             case.block_size, case.compress_ratio, case.rms_norm_eps, y.data_ptr()]
 
 
-@pytest.mark.parametrize("R,T,C", [(2, 4096, 128), (1, 8192, 512), (8, 131072, 128)])
-def test_static_entry_matches_workspace_entry_on_two_calls(kvc, R, T, C):
-    # outputs split between CTAs, so the scratch (partials + counters) is used
+@pytest.mark.parametrize("R,T,C,route", [(2, 4096, 128, "streamk"), (1, 8192, 512, "streamk"),
+                                         (8, 131072, 128, "streamk"), (2, 4096, 128, "auto")])
+def test_static_entry_matches_workspace_entry_on_two_calls(kvc, R, T, C, route):
+    # the stream-K route splits outputs between CTAs, so the scratch (partial
+    # states + arrival counters) is used
     case = inputs.make_case(R, T, C, seed=inputs.BASE_SEED + 4242 + C, kv_fill=5)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -58,7 +60,8 @@ def test_static_entry_matches_workspace_entry_on_two_calls(kvc, R, T, C):
 
     ws = torch.zeros(kvc.kvc_workspace_bytes(N), dtype=torch.uint8, device="cuda")
     y_ref = torch.empty((N, 512), dtype=torch.float32, device="cuda")
-    st = kvc.kvc_compress(*_raw_args(d, case, y_ref, sp), ws.data_ptr(), ws.numel(), 0, sp)
+    flags = kvc.make_flags(route)
+    st = kvc.kvc_compress(*_raw_args(d, case, y_ref, sp), ws.data_ptr(), ws.numel(), flags, sp)
     assert st == kvc.KVC_OK
     assert kvc.kvc_get_device_error(sp) == 0
     kv_ref = d["kv_cache"].cpu().numpy()
@@ -68,7 +71,7 @@ def test_static_entry_matches_workspace_entry_on_two_calls(kvc, R, T, C):
     for call in range(2):
         d["kv_cache"].copy_(torch.from_numpy(case.kv_cache))
         y = torch.full((N, 512), float("nan"), dtype=torch.float32, device="cuda")
-        st = kvc.kvc_compress_static(*_raw_args(d, case, y, sp), 0, sp)
+        st = kvc.kvc_compress_static(*_raw_args(d, case, y, sp), flags, sp)
         assert st == kvc.KVC_OK, f"call {call}: {kvc.kvc_error_string(st)}"
         assert kvc.kvc_get_device_error(sp) == 0
         y_np = y.cpu().numpy()
@@ -83,11 +86,12 @@ def test_static_entry_takes_no_device_memory_per_call(kvc):
     d = to_device(case)
     y = torch.empty((case.num_outputs, 512), dtype=torch.float32, device="cuda")
     args = _raw_args(d, case, y, sp)
-    assert kvc.kvc_compress_static(*args, 0, sp) == kvc.KVC_OK   # first call: set-up
+    flags = kvc.make_flags("streamk")
+    assert kvc.kvc_compress_static(*args, flags, sp) == kvc.KVC_OK   # first call: set-up
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     for _ in range(3):
-        assert kvc.kvc_compress_static(*args, 0, sp) == kvc.KVC_OK
+        assert kvc.kvc_compress_static(*args, flags, sp) == kvc.KVC_OK
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0
