@@ -400,7 +400,9 @@ def main():
             n_steps = 2000 if cs.state_bits.nbytes < 100 * 2 ** 20 else 600
             tc, _ = time_device(kvc, cs, device, n_steps, 20)
             b = bytes_for(cs)
+            sctas, sclu, _, _ = kvc.kvc_query_launch(cs.num_outputs, cs.compress_ratio)
             sweep.append({"shape": cs.name, "outputs": cs.num_outputs, "bytes": b,
+                          "ctas": sctas, "cluster_size": sclu,
                           "us_per_call": round(tc * 1e6, 3),
                           "gb_s": round(b / tc / 1e9, 1),
                           "pct_of_peak": round(100 * b / tc / 1e9 / peak, 1)})
@@ -440,7 +442,8 @@ def main():
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": traffic, "kernel": "kvc_compress_kernel",
+                     "traffic": traffic,
+                     "kernel": f"kvc_cluster_kernel<{cluster}>" if cluster else "kvc_streamk_kernel",
                      "algorithmic_bytes_per_launch": per_call_bytes},
         "gpu_launches": args.steps,
         "clocks": clocks,
