@@ -9,7 +9,7 @@
  *
  *   for every boundary token b = boundary_token_indices[n]:
  *     r = token_to_req[b], p = positions[b], window t = p-C+1 .. p;
- *     row(t) = block_table[r, t/8] * 8 + t%8 of state_cache (block_size 8);
+ *     row(t) = block_table[r, t/B] * B + t%B of state_cache (block_size B);
  *     c_d = sum_t softmax_t(score[row(t), d]) * value[row(t), d], d < 512
  *           (softmax along the window, separately per dimension);
  *     y = c * (mean(c^2) + eps)^-1/2 * rms_norm_weight;
@@ -39,8 +39,10 @@ extern "C" {
 typedef enum {
   KVC_OK = 0,
   KVC_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, small workspace */
-  KVC_ERR_UNSUPPORTED = 2,  /* block_size != 8, C not a multiple of 8, or (device)
-                               a window that does not start on an 8-row block */
+  KVC_ERR_UNSUPPORTED = 2,  /* block_size < 8; a cluster size the problem or device
+                               cannot take; the stream-K route asked for with
+                               block_size != 8 or C not a multiple of 8, or (device,
+                               stream-K route) a window not starting on an 8-row block */
   KVC_ERR_CUDA = 3,         /* a CUDA runtime call failed */
   KVC_ERR_BAD_INDEX = 4,    /* (device) an index outside its array */
   KVC_ERR_TIMEOUT = 5,      /* (device) a pipeline wait ran past its limit */
@@ -74,8 +76,9 @@ size_t kvc_workspace_bytes(int64_t num_outputs);
 /*
  * Compress every boundary token's window into its kv_cache slot.
  *
- * state_cache      bf16 [num_state_blocks, 8, 1024], contiguous, 16-byte
- *                  aligned; row columns 0..511 are values, 512..1023 scores.
+ * state_cache      bf16 [num_state_blocks, block_size, 1024], contiguous,
+ *                  16-byte aligned; row columns 0..511 are values, 512..1023
+ *                  scores.
  * token_to_req     int32 [num_tokens]: request of each token.
  * positions        int64 [num_tokens]: position of each token in its request.
  * boundary_token_indices  int64 [num_outputs]: token index b of each output.
@@ -88,7 +91,10 @@ size_t kvc_workspace_bytes(int64_t num_outputs);
  *                  negative slot skips that output.
  * kv_cache         uint8 [num_kv_pages, 37376], 16-byte aligned; written in
  *                  place, only at the 576 + 8 bytes of each written slot.
- * block_size       must be 8.   compress_ratio  C, a positive multiple of 8.
+ * block_size       B >= 8 rows per physical block (the write-up's is 8).
+ * compress_ratio   C >= 1 (the write-up's are 128, 256, 512).  Windows may
+ *                  start at any position p - C + 1 >= 0 (the benchmark's start
+ *                  on a block boundary).
  * rms_norm_eps     finite, >= 0 (the write-up's default is 1e-6).
  * y_out            optional fp32 [num_outputs, 512], 8-byte aligned, or NULL:
  *                  receives the RMS-normalised vector y of each output (before

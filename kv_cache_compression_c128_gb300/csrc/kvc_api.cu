@@ -115,11 +115,16 @@ int auto_cluster_size(const DeviceInfo& d, int64_t N, int64_t K) {
   return best;
 }
 
-bool pick_route(const DeviceInfo& d, int64_t N, int64_t K, uint32_t flags, Route* r) {
+// Route for N outputs of K chunks.  `aligned` = block_size 8 and C a multiple
+// of 8 (the stream-K route handles only those; the window start is checked
+// on the device).
+bool pick_route(const DeviceInfo& d, int64_t N, int64_t K, bool aligned, uint32_t flags,
+                Route* r) {
   const int forced_count = static_cast<int>(flags & KVC_FLAG_GRID_MASK);
   const int forced_s = static_cast<int>((flags & KVC_FLAG_CLUSTER_MASK) >> KVC_FLAG_CLUSTER_SHIFT);
   const int S = (flags & KVC_FLAG_STREAM_K) ? 0 : (forced_s ? forced_s : auto_cluster_size(d, N, K));
   if (S == 0) {  // stream-K: asked for, or no cluster size fits this device
+    if (!aligned) return false;
     const int64_t units = N * K;
     const int64_t cap = static_cast<int64_t>(d.sms) * d.streamk_ctas_per_sm;
     int64_t g = forced_count ? forced_count : cap;
@@ -150,14 +155,15 @@ size_t kvc_workspace_bytes(int64_t num_outputs) {
 kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio, uint32_t flags,
                             int32_t* ctas, int32_t* cluster_size, int32_t* threads,
                             int32_t* smem_bytes) {
-  if (num_outputs < 0 || compress_ratio <= 0 || compress_ratio % kvc::kBlockRows != 0 ||
-      (flags & ~KVC_FLAG_ALL) != 0)
+  if (num_outputs < 0 || compress_ratio <= 0 || (flags & ~KVC_FLAG_ALL) != 0)
     return KVC_ERR_INVALID_ARG;
   DeviceInfo d;
   const kvc_status st = device_info(&d);
   if (st != KVC_OK) return st;
   Route r{false, 0, 1};
-  if (num_outputs > 0 && !pick_route(d, num_outputs, compress_ratio / kvc::kBlockRows, flags, &r))
+  const int64_t K = (compress_ratio + kvc::kBlockRows - 1) / kvc::kBlockRows;
+  if (num_outputs > 0 &&
+      !pick_route(d, num_outputs, K, compress_ratio % kvc::kBlockRows == 0, flags, &r))
     return KVC_ERR_UNSUPPORTED;
   if (ctas) *ctas = num_outputs > 0 ? (r.stream_k ? r.count : r.count * r.cluster) : 0;
   if (cluster_size) *cluster_size = r.stream_k ? 0 : r.cluster;
@@ -179,8 +185,8 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
                         float* y_out, void* workspace, size_t workspace_bytes, uint32_t flags,
                         void* stream) {
   if (num_outputs < 0 || (flags & ~KVC_FLAG_ALL) != 0) return KVC_ERR_INVALID_ARG;
-  if (block_size != kvc::kBlockRows) return KVC_ERR_UNSUPPORTED;
-  if (compress_ratio <= 0 || compress_ratio % kvc::kBlockRows != 0) return KVC_ERR_UNSUPPORTED;
+  if (block_size < kvc::kBlockRows) return KVC_ERR_UNSUPPORTED;
+  if (compress_ratio <= 0) return KVC_ERR_INVALID_ARG;
   if (!std::isfinite(rms_norm_eps) || rms_norm_eps < 0.f) return KVC_ERR_INVALID_ARG;
   if (num_outputs == 0) return KVC_OK;
   if (!state_cache || !token_to_req || !positions || !boundary_token_indices || !block_table ||
@@ -223,7 +229,8 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
   p.num_pages = num_kv_pages;
   p.y_out = y_out;
   p.compress_ratio = compress_ratio;
-  p.blocks_per_output = compress_ratio / kvc::kBlockRows;
+  p.block_size = block_size;
+  p.blocks_per_output = (compress_ratio + kvc::kBlockRows - 1) / kvc::kBlockRows;
   p.num_units = num_outputs * p.blocks_per_output;
   p.eps = rms_norm_eps;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -233,7 +240,8 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
   p.error = d.error_word;
 
   Route r;
-  if (!pick_route(d, num_outputs, p.blocks_per_output, flags, &r)) return KVC_ERR_UNSUPPORTED;
+  const bool aligned = block_size == kvc::kBlockRows && compress_ratio % kvc::kBlockRows == 0;
+  if (!pick_route(d, num_outputs, p.blocks_per_output, aligned, flags, &r)) return KVC_ERR_UNSUPPORTED;
   p.cluster_size = r.cluster;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e =

@@ -6,10 +6,14 @@
 // streamed as in "Online Softmax: Streaming Away the Window", then RMSNorm,
 // NOPE quantisation, RoPE and the packed slot store.
 //
-// Work decomposition.  Output n is handled by one thread-block cluster of S
-// CTAs (S = 1, 2, 4, 8, 16); rank j streams blocks [j K/S, (j+1) K/S) of the
-// window (K = C/8 blocks of 16 KiB).  Persistent clusters take contiguous,
-// equal ranges of outputs, so every CTA streams the same number of blocks.
+// Work decomposition.  A window of C rows is cut into K = ceil(C/8) chunks of
+// 8 rows (the last may be shorter); with the benchmark's block-aligned
+// windows and block_size 8 a chunk is exactly one 16 KiB physical block, in
+// general it is at most two runs of consecutive physical rows (block_size >=
+// 8).  Output n is handled by one thread-block cluster of S CTAs (S = 1, 2,
+// 4, 8, 16); rank j streams chunks [j K/S, (j+1) K/S).  Persistent clusters
+// take contiguous, equal ranges of outputs, so every CTA streams the same
+// number of chunks.
 //
 // Inside a CTA (320 threads):
 //   warp 9  resolver: turns units into physical blocks (boundary index ->
@@ -45,11 +49,12 @@ constexpr int kResolverWarp = kConsumerWarps + 1;
 constexpr int kFifoChunk = 32;
 
 struct alignas(16) FifoEntry {
-  long long blk;    // physical block, -1 if unresolved
-  long long slot;   // output slot (first unit of an output only)
-  long long pc;     // compressed position (first unit of an output only)
-  int first;        // first unit of its output in this CTA
-  int piece;        // output index relative to the cluster's first output
+  long long row1, row2;  // physical row runs of the chunk (row1 < 0: unresolved)
+  long long slot;        // output slot (first unit of an output only)
+  long long pc;          // compressed position (first unit of an output only)
+  int n1, n2;            // rows in each run
+  int first;             // first unit of its output in this CTA
+  int piece;             // output index relative to the cluster's first output
 };
 
 template <int S>
@@ -68,7 +73,7 @@ struct ClusterShared {
   float recv_bad[S > 1 ? S : 1];
   float ss_recv[kMaxFinalizers];
   FinalScratch fs;
-  uint32_t stage_ok[kStages];
+  uint32_t stage_rows[kStages];  // valid rows in each stage (0: unresolved chunk)
   int abort_flag;
 };
 
@@ -84,12 +89,17 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int6
   const int lane = threadIdx.x & 31;
   for (int64_t c = 0; c * kFifoChunk < units; ++c) {
     const int64_t i = c * kFifoChunk + lane;
-    FifoEntry e{-1, -1, -1, 0, 0};
+    FifoEntry e{-1, -1, -1, -1, 0, 0, 0, 0};
     if (i < units) {
       const int64_t q = i / kj;
       const int kk = static_cast<int>(i - q * kj);
       MetaRec rec;
-      resolve_unit(p, n0 + q, k_lo + kk, kk == 0, e.blk, rec);
+      ChunkRuns cr;
+      resolve_chunk(p, n0 + q, k_lo + kk, kk == 0, cr, rec);
+      e.row1 = cr.row1;
+      e.row2 = cr.row2;
+      e.n1 = cr.n1;
+      e.n2 = cr.n2;
       e.slot = rec.slot;
       e.pc = rec.pc;
       e.first = (kk == 0);
@@ -147,14 +157,17 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
         m.slot = e.slot;
         m.pc = e.pc;
       }
-      if (e.blk >= 0) {
-        sh.stage_ok[stage] = 1;
-        mbar_arrive_expect_tx(&sh.full_bar[stage], kBlockBytes);
-        bulk_copy_g2s(ring + static_cast<size_t>(stage) * kBlockBytes,
-                      p.state + e.blk * (kBlockRows * kRowElems), kBlockBytes, &sh.full_bar[stage],
-                      policy);
+      if (e.row1 >= 0) {
+        constexpr uint32_t kRowBytes = kRowElems * 2;
+        uint8_t* dst = ring + static_cast<size_t>(stage) * kBlockBytes;
+        sh.stage_rows[stage] = static_cast<uint32_t>(e.n1 + e.n2);
+        mbar_arrive_expect_tx(&sh.full_bar[stage], (e.n1 + e.n2) * kRowBytes);
+        bulk_copy_g2s(dst, p.state + e.row1 * kRowElems, e.n1 * kRowBytes, &sh.full_bar[stage], policy);
+        if (e.n2 > 0)
+          bulk_copy_g2s(dst + e.n1 * kRowBytes, p.state + e.row2 * kRowElems, e.n2 * kRowBytes,
+                        &sh.full_bar[stage], policy);
       } else {
-        sh.stage_ok[stage] = 0;
+        sh.stage_rows[stage] = 0;
         mbar_arrive(&sh.full_bar[stage]);
       }
       issued |= 1u << stage;
@@ -211,8 +224,11 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
           sn = __ldg(p.cos_sin + meta.pc * kRopeDim + kRopeDim / 2 + jp);
         }
       }
-      if (ready && sh.stage_ok[stage]) {
+      const uint32_t rows = ready ? sh.stage_rows[stage] : 0u;
+      if (rows == kBlockRows) {
         fold_block(ring + static_cast<size_t>(stage) * kBlockBytes, t, s);
+      } else if (rows > 0) {
+        fold_rows(ring + static_cast<size_t>(stage) * kBlockBytes, t, s, static_cast<int>(rows));
       } else {
         bad = true;
       }

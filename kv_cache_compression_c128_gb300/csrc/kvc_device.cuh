@@ -329,6 +329,99 @@ __device__ __forceinline__ void resolve_unit(const Params& p, int64_t n, int k, 
   }
 }
 
+// Rows of window chunk k (rows t0 + 8k .. t0 + 8k + nr - 1 of the request, nr
+// = min(8, C - 8k)) as at most two runs of consecutive physical rows: the
+// part in logical block l1 = (t0 + 8k) / B from offset o1, and the rest at the
+// start of block l1 + 1 (block_size B >= 8, so a chunk never touches three
+// blocks).  Row indices count rows of state_cache ([num_blocks * B, 1024]).
+struct ChunkRuns {
+  long long row1, row2;  // first physical row of each run (row1 < 0: bad chunk)
+  int n1, n2;            // rows in each run (n2 = 0: one run)
+};
+
+// Resolve chunk k of output n for the cluster route (any window start, any
+// C >= 1, any B >= 8), and, when want_meta, the output's slot and compressed
+// position.  All loads of one level are issued together: the chain before
+// the first copy is boundary index -> (request, position, slot) -> one or
+// two block-table entries.
+__device__ __forceinline__ void resolve_chunk(const Params& p, int64_t n, int k, bool want_meta,
+                                              ChunkRuns& cr, MetaRec& rec) {
+  cr = ChunkRuns{-1, -1, 0, 0};
+  rec = MetaRec{-1, -1};
+  const int64_t b = __ldg(p.bti + n);
+  if (b < 0 || b >= p.num_tokens) { record_error(p.error, kErrBadIndex); return; }
+  const int64_t r = __ldg(p.token_to_req + b);
+  const int64_t pos = __ldg(p.positions + b);
+  const int64_t slot = want_meta ? __ldg(p.slot_map + (p.slot_by_token ? b : n)) : -1;
+  const int64_t C = p.compress_ratio, B = p.block_size;
+  const int64_t t0 = pos - C + 1;
+  if (r < 0 || r >= p.num_reqs || t0 < 0) { record_error(p.error, kErrBadIndex); return; }
+  const int64_t first = t0 + static_cast<int64_t>(kBlockRows) * k;
+  const int64_t left = C - static_cast<int64_t>(kBlockRows) * k;
+  const int nr = static_cast<int>(left < kBlockRows ? left : kBlockRows);
+  const int64_t l1 = first / B, o1 = first - l1 * B;
+  const int n1 = static_cast<int>(B - o1 < nr ? B - o1 : nr);
+  const int n2 = nr - n1;
+  if (l1 + (n2 > 0 ? 1 : 0) >= p.max_blocks) { record_error(p.error, kErrBadIndex); return; }
+  const int64_t g1 = __ldg(p.block_table + r * p.max_blocks + l1);
+  const int64_t g2 = n2 > 0 ? __ldg(p.block_table + r * p.max_blocks + l1 + 1) : 0;
+  if (g1 < 0 || g1 >= p.num_blocks || g2 < 0 || g2 >= p.num_blocks) {
+    record_error(p.error, kErrBadIndex);
+    return;
+  }
+  if (want_meta) {
+    const int64_t pc = (pos / C) * C;
+    if (pc >= p.num_positions || (slot >= 0 && (slot / kSlotsPerPage) >= p.num_pages)) {
+      record_error(p.error, kErrBadIndex);
+      return;
+    }
+    rec.slot = slot;
+    rec.pc = pc;
+  }
+  cr.row1 = g1 * B + o1;
+  cr.n1 = n1;
+  cr.row2 = n2 > 0 ? g2 * B : -1;
+  cr.n2 = n2;
+}
+
+// fold_block for a chunk holding only its first `nrows` (1..7) rows: the
+// missing rows act as score -inf, value 0 (they add nothing and do not move
+// the maximum).
+__device__ __forceinline__ void fold_rows(const uint8_t* blk, int t, SoftmaxState& s, int nrows) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(blk);
+  uint32_t sw[kBlockRows], vw[kBlockRows];
+#pragma unroll
+  for (int r = 0; r < kBlockRows; ++r) {
+    const bool in = r < nrows;
+    sw[r] = in ? w[r * (kRowElems / 2) + (kHeadDim / 2) + t] : 0xFF80FF80u;  // bf16 -inf pair
+    vw[r] = in ? w[r * (kRowElems / 2) + t] : 0u;
+  }
+  const uint32_t mx = bf16x2_max(bf16x2_max(bf16x2_max(sw[0], sw[1]), bf16x2_max(sw[2], sw[3])),
+                                 bf16x2_max(bf16x2_max(sw[4], sw[5]), bf16x2_max(sw[6], sw[7])));
+  const float nm0 = fmaxf(s.m0, bf16_lo(mx));
+  const float nm1 = fmaxf(s.m1, bf16_hi(mx));
+  const float r0 = fast_ex2((s.m0 - nm0) * kLog2e);
+  const float r1 = fast_ex2((s.m1 - nm1) * kLog2e);
+  float d0 = 0.f, d1 = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int r = 0; r < kBlockRows; ++r) {
+    if (r < nrows) {
+      const float e0 = fast_ex2(fmaf(bf16_lo(sw[r]), kLog2e, -nm0 * kLog2e));
+      const float e1 = fast_ex2(fmaf(bf16_hi(sw[r]), kLog2e, -nm1 * kLog2e));
+      d0 += e0;
+      d1 += e1;
+      a0 = fmaf(e0, bf16_lo(vw[r]), a0);
+      a1 = fmaf(e1, bf16_hi(vw[r]), a1);
+    }
+  }
+  s.d0 = fmaf(s.d0, r0, d0);
+  s.d1 = fmaf(s.d1, r1, d1);
+  s.a0 = fmaf(s.a0, r0, a0);
+  s.a1 = fmaf(s.a1, r1, a1);
+  s.m0 = nm0;
+  s.m1 = nm1;
+}
+
 // ---- finaliser ------------------------------------------------------------------------
 
 // Shared-memory scratch of the finaliser (one per CTA).

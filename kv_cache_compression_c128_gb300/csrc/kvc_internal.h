@@ -58,8 +58,9 @@ struct Params {
   int64_t num_pages;
   float* y_out;                   // optional
   int compress_ratio;             // C
-  int blocks_per_output;          // K = C / 8
-  int64_t num_units;              // U = N * K: one unit = one 8-row block
+  int block_size;                 // B: rows per physical state block
+  int blocks_per_output;          // K = ceil(C / 8): 8-row chunks per window
+  int64_t num_units;              // U = N * K: one unit = one 8-row chunk
   float eps;
   int cluster_size;               // cluster route: CTAs per output (S)
   float* partials;                // [2 * max_ctas][kPartialFloats]

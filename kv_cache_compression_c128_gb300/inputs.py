@@ -122,13 +122,19 @@ def _cos_sin_table(num_positions: int) -> np.ndarray:
 def make_case(num_reqs: int, total_tokens: int, compress_ratio: int, *,
               seed: int, block_size: int = BLOCK_SIZE,
               lengths: Optional[Sequence[int]] = None,
-              kv_fill: Optional[int] = None, name: str = "") -> Case:
+              kv_fill: Optional[int] = None, name: str = "",
+              boundaries_per_req: Optional[int] = None) -> Case:
     """Build one seeded synthetic call.
 
-    ``lengths`` (per-request token counts, each a multiple of
-    ``compress_ratio`` and of ``block_size``) defaults to equal requests.
-    ``kv_fill``: None -> zero-filled kv_cache; an int -> a seeded byte pattern
-    drawn from that seed (used to check that unwritten bytes stay untouched).
+    ``lengths`` (per-request token counts, each a multiple of ``block_size``;
+    of ``compress_ratio`` too unless ``boundaries_per_req`` is given) defaults
+    to equal requests.  Boundary tokens are those with ``(p + 1) % C == 0``,
+    as in the benchmark; with ``boundaries_per_req`` set they are instead
+    that many distinct positions per request drawn uniformly from
+    ``[C - 1, L - 1]`` (windows at arbitrary offsets, for the general-window
+    tests).  ``kv_fill``: None -> zero-filled kv_cache; an int -> a seeded
+    byte pattern drawn from that seed (to check that unwritten bytes stay
+    untouched).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     R, T, C, B = num_reqs, total_tokens, compress_ratio, block_size
@@ -137,7 +143,9 @@ def make_case(num_reqs: int, total_tokens: int, compress_ratio: int, *,
         lengths = [T // R] * R
     lengths = np.asarray(lengths, dtype=np.int64)
     assert lengths.shape == (R,) and int(lengths.sum()) == T
-    assert all(int(L) % B == 0 and int(L) % C == 0 for L in lengths)
+    assert all(int(L) % B == 0 for L in lengths)
+    if boundaries_per_req is None:
+        assert all(int(L) % C == 0 for L in lengths)
 
     num_blocks = T // B
     state = rng.standard_normal((num_blocks, B, STATE_WIDTH), dtype=np.float32)
@@ -147,6 +155,7 @@ def make_case(num_reqs: int, total_tokens: int, compress_ratio: int, *,
     perm = rng.permutation(num_blocks).astype(np.int32)
     max_blocks = int(lengths.max()) // B
     block_table = np.full((R, max_blocks), -1, dtype=np.int32)
+    assert num_blocks == T // B
     token_to_req = np.empty(T, dtype=np.int32)
     positions = np.empty(T, dtype=np.int64)
     start_tok = 0
@@ -159,7 +168,17 @@ def make_case(num_reqs: int, total_tokens: int, compress_ratio: int, *,
         start_tok += L
         start_blk += nb
 
-    bti = np.nonzero((positions + 1) % C == 0)[0].astype(np.int64)
+    if boundaries_per_req is None:
+        bti = np.nonzero((positions + 1) % C == 0)[0].astype(np.int64)
+    else:
+        picks = []
+        start = 0
+        for L in lengths.tolist():
+            k = min(boundaries_per_req, L - C + 1)
+            pos = rng.choice(np.arange(C - 1, L), size=k, replace=False)
+            picks.append(start + np.sort(pos))
+            start += L
+        bti = np.concatenate(picks).astype(np.int64)
     N = int(bti.shape[0])
     weight = (1.0 + 0.1 * rng.standard_normal(HEAD_DIM)).astype(np.float32)
     csc = _cos_sin_table(int(lengths.max()))

@@ -72,9 +72,10 @@ _GOOD = dict(state_cache=0x10000, num_state_blocks=1024, token_to_req=0x20000,
 
 
 @pytest.mark.parametrize("change,status", [
-    (dict(block_size=16), 2),
-    (dict(compress_ratio=100), 2),
-    (dict(compress_ratio=0), 2),
+    (dict(block_size=4), 2),
+    (dict(block_size=0), 2),
+    (dict(compress_ratio=0), 1),
+    (dict(compress_ratio=-8), 1),
     (dict(num_outputs=-1), 1),
     (dict(flags=1 << 28), 1),
     (dict(rms_norm_eps=float("nan")), 1),
@@ -100,7 +101,7 @@ def test_zero_outputs_is_a_no_op(kvc):
 
 def test_query_launch_rejects_bad_arguments(kvc):
     with pytest.raises(kvc.KvcError):
-        kvc.kvc_query_launch(64, 100)
+        kvc.kvc_query_launch(64, 0)
     with pytest.raises(kvc.KvcError):
         kvc.kvc_query_launch(-1, 128)
     with pytest.raises(kvc.KvcError):

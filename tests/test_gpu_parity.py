@@ -213,11 +213,14 @@ def test_window_before_sequence_start(kvc, oracle_mod):
     _expect_device_error(kvc, case, 4, [2], oracle_mod)
 
 
-def test_unaligned_window_is_unsupported(kvc, oracle_mod):
+def test_unaligned_window_stream_k_unsupported_cluster_exact(kvc, oracle_mod):
     case = inputs.make_case(1, 1024, 64, seed=89, kv_fill=90)
     case.boundary_token_indices = case.boundary_token_indices.copy()
     case.boundary_token_indices[3] += 1          # window starts at an odd row
-    _expect_device_error(kvc, case, 2, [3], oracle_mod)
+    # the stream-K route handles only block-aligned windows: reported, skipped
+    _expect_device_error(kvc, case, 2, [3], oracle_mod, grid=kvc.make_flags("streamk"))
+    # the cluster route computes it like any other window
+    check_case(oracle_mod, case)
 
 
 def test_slot_and_position_out_of_range(kvc, oracle_mod):
@@ -235,3 +238,33 @@ def test_slot_and_position_out_of_range(kvc, oracle_mod):
     assert err2 == 0
     case2.cos_sin_cache = case2.cos_sin_cache[:1984].copy()    # pc = 1984 now out of range
     _expect_device_error(kvc, case2, 4, [last], oracle_mod)
+
+
+# ---- general windows: any start, any C >= 1, block_size >= 8 ------------------
+
+GENERAL = [  # (num_reqs, total_tokens, C, block_size, boundaries per request)
+    (2, 1024, 37, 8, 20),
+    (2, 1024, 100, 16, 20),
+    (1, 2048, 1, 8, 40),
+    (3, 1440, 5, 24, 16),
+    (2, 4096, 300, 64, 12),
+    (1, 4096, 128, 8, 25),     # the benchmark's C at unaligned window starts
+    (1, 4096, 512, 32, 10),
+]
+
+
+@pytest.mark.parametrize("R,T,C,B,nb", GENERAL)
+@pytest.mark.parametrize("S", [0, 1, 2, 4, 8, 16])
+def test_general_windows(kvc, oracle_mod, R, T, C, B, nb, S):
+    if S > -(-C // 8):
+        pytest.skip("cluster larger than the window's chunk count")
+    case = inputs.make_case(R, T, C, seed=inputs.BASE_SEED + 700 + C + B, block_size=B,
+                            boundaries_per_req=nb, kv_fill=13)
+    check_case(oracle_mod, case, flags=kvc.make_flags("cluster", 0, S) if S else 0)
+
+
+def test_general_windows_not_on_the_stream_k_route(kvc):
+    case = inputs.make_case(1, 1024, 100, seed=5, block_size=16, boundaries_per_req=4)
+    with pytest.raises(kvc.KvcError) as ei:
+        run_gpu(case, flags=kvc.make_flags("streamk"))
+    assert ei.value.status == kvc.KVC_ERR_UNSUPPORTED
