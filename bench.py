@@ -262,6 +262,43 @@ def time_device(kvc, case, device, steps: int, warmup: int, sampler=None,
     return elapsed / steps, elapsed
 
 
+def time_reader(kvc, case, device, steps: int = 2000):
+    """Per-call time of kvc_dequantize reading back every slot of `case`
+    (fp32 and bf16 outputs), after one compression fills the cache."""
+    import torch
+
+    states, d = _tensors(case, device, 1)
+    kvc.c128_256_512_compress(states[0], block_size=case.block_size,
+                              compress_ratio=case.compress_ratio, **d)
+    slots = torch.from_numpy(case.kv_slot_mapping[case.boundary_token_indices]).to(device)
+    M = slots.numel()
+    res = {}
+    for name, dtype, width in (("f32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        out = torch.empty((M, 512), dtype=dtype, device=device)
+        stream = torch.cuda.Stream(device)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                kvc.dequantize(d["kv_cache"], slots, dtype=dtype, out=out, stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(200):
+                    kvc.dequantize(d["kv_cache"], slots, dtype=dtype, out=out, stream=stream)
+            g.replay()
+            torch.cuda.synchronize(device)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(max(1, steps // 200)):
+                g.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize(device)
+        t = ev0.elapsed_time(ev1) / 1e3 / (max(1, steps // 200) * 200)
+        b = M * (576 + 8 + 8) + M * 512 * width
+        res[name] = {"us_per_call": round(t * 1e6, 3), "bytes": b, "gb_s": round(b / t / 1e9, 1)}
+    assert kvc.kvc_get_device_error(torch.cuda.current_stream(device).cuda_stream) == 0
+    return {"slots": M, **res}
+
+
 def time_e2e(kvc, case, device, steps: int, warmup: int):
     """Seconds per call through the public API from pinned host buffers:
     H2D of every input, the call, D2H of kv_cache, all inside the region."""
@@ -324,9 +361,12 @@ def time_oracle(case, max_outputs: int):
 
 
 def bytes_for(case, n_outputs=None) -> int:
+    """Algorithmic bytes of a call: state rows, block-table entries (one per
+    8-row chunk of the window, two where a chunk straddles blocks; counted
+    as one), per-output metadata, one cos/sin row, the weights, the slot."""
     n = case.num_outputs if n_outputs is None else n_outputs
     c = case.compress_ratio
-    return n * c * 2048 + n * (c // case.block_size) * 4 + n * 28 + n * 256 + 2048 + n * 584
+    return n * c * 2048 + n * (-(-c // 8)) * 4 + n * 28 + n * 256 + 2048 + n * 584
 
 
 # ---- main ------------------------------------------------------------------------
@@ -391,12 +431,16 @@ def main():
                "us_per_call": round(t_e2e * 1e6, 2), "steps": e_steps,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    reader = time_reader(kvc, case, device) if rank == 0 else None
+
     sweep = None
     if not args.no_sweep and rank == 0:
         sweep = []
-        shapes = [(i, inputs.bench_case) for i in range(12)]
-        for i, make in shapes + [(c, None) for c in (128, 256, 512)]:
-            cs = inputs.bench_case(i) if make else inputs.ragged_case(i)
+        makers = ([lambda i=i: inputs.bench_case(i) for i in range(12)]
+                  + [lambda c=c: inputs.ragged_case(c) for c in (128, 256, 512)]
+                  + [lambda: inputs.general_window_case(128, 16)])
+        for make in makers:
+            cs = make()
             n_steps = 2000 if cs.state_bits.nbytes < 100 * 2 ** 20 else 600
             tc, _ = time_device(kvc, cs, device, n_steps, 20)
             b = bytes_for(cs)
@@ -448,6 +492,7 @@ def main():
         "gpu_launches": args.steps,
         "clocks": clocks,
         "e2e": e2e,
+        "reader": reader,
         "cpu_baseline": cpu,
         "sweep": sweep,
         "kernel_source_hash": kernel_source_hash(),

@@ -125,6 +125,32 @@ kvc_status kvc_compress(
     float* y_out, void* workspace, size_t workspace_bytes,
     uint32_t flags, void* stream);
 
+/* Output element types of kvc_dequantize. */
+#define KVC_DTYPE_F32 0
+#define KVC_DTYPE_BF16 1
+
+/*
+ * Read packed slots back as 512-vectors (the reader side of the cache: the
+ * attention that consumes the compressed keys).  Layout of "Gather and
+ * Scatter" in the write-up; values of its quantisation equation ("How One
+ * Output Is Produced"):
+ *   out[m, d] = q_d * 2^(scale[d / 64] - 127)   d < 448, q_d the int8 code,
+ *   out[m, d] = the stored bf16 RoPE value       d >= 448,
+ * computed exactly (a power-of-two scaling) and written as fp32
+ * (out_dtype KVC_DTYPE_F32, out 16-byte aligned, float [num_slots, 512]) or
+ * bf16 (KVC_DTYPE_BF16, out 8-byte aligned, [num_slots, 512]; every such
+ * value is exactly representable in bf16 unless it overflows).
+ *
+ * kv_cache  uint8 [num_kv_pages, 37376], 16-byte aligned, read only.
+ * slots     int64 [num_slots]: slot m to read; a negative slot yields zeros;
+ *           a slot beyond the last page yields zeros and records
+ *           KVC_ERR_BAD_INDEX in the device error word.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+kvc_status kvc_dequantize(const uint8_t* kv_cache, int64_t num_kv_pages,
+                          const int64_t* slots, int64_t num_slots, void* out,
+                          int32_t out_dtype, void* stream);
+
 /*
  * kvc_compress without a workspace argument, for callers that cannot
  * allocate device memory: plugins that are handed only their input and

@@ -24,7 +24,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(_LIB_DIR, "libkvc.so")
-_SOURCES = ["kvc_cluster.cu", "kvc_streamk.cu", "kvc_api.cu", "kvc_static.cu"]
+_SOURCES = ["kvc_cluster.cu", "kvc_streamk.cu", "kvc_reader.cu", "kvc_api.cu", "kvc_static.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 KVC_OK = 0
@@ -35,6 +35,8 @@ KVC_ERR_BAD_INDEX = 4
 KVC_ERR_TIMEOUT = 5
 KVC_ERR_SCRATCH_LIMIT = 6
 KVC_FLAG_GRID_MASK = 0xFFFF
+KVC_DTYPE_F32 = 0
+KVC_DTYPE_BF16 = 1
 KVC_FLAG_CLUSTER_SHIFT = 16
 KVC_FLAG_STREAM_K = 1 << 24
 
@@ -134,6 +136,8 @@ def lib():
                 P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P, I64,
                 I32, I32, ctypes.c_float, P, U32, P]
             L.kvc_compress_static.restype = ctypes.c_int
+            L.kvc_dequantize.argtypes = [P, I64, P, I64, P, I32, P]
+            L.kvc_dequantize.restype = ctypes.c_int
             L.kvc_query_launch.argtypes = [I64, I32, U32, P, P, P, P]
             L.kvc_query_launch.restype = ctypes.c_int
             L.kvc_get_device_error.argtypes = [P, P]
@@ -214,6 +218,43 @@ def kvc_compress_static(state_cache, num_state_blocks, token_to_req, positions, 
         max_blocks_per_req, v(rms_norm_weight), v(cos_sin_cache), num_positions,
         v(kv_slot_mapping), slot_mapping_len, v(kv_cache), num_kv_pages, block_size,
         compress_ratio, ctypes.c_float(rms_norm_eps), v(y_out), flags, v(stream)))
+
+
+def kvc_dequantize(kv_cache, num_kv_pages, slots, num_slots, out, out_dtype, stream) -> int:
+    """Decode slots back to vectors (raw integer pointers); returns the status."""
+    v = ctypes.c_void_p
+    return int(lib().kvc_dequantize(v(kv_cache), num_kv_pages, v(slots), num_slots, v(out),
+                                    int(out_dtype), v(stream)))
+
+
+# ---- torch-facing wrappers ----------------------------------------------------
+
+def dequantize(kv_cache, slots, dtype=None, out=None, stream=None):
+    """Read slots of a packed kv_cache back as [len(slots), 512] vectors
+    (torch.float32 or torch.bfloat16) on the cache's device."""
+    import torch
+
+    dtype = torch.float32 if dtype is None else dtype
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("dtype must be torch.float32 or torch.bfloat16")
+    dev = kv_cache.device
+    if dev.type != "cuda":
+        raise ValueError("kv_cache must be a CUDA tensor (there is no CPU path)")
+    _check(kv_cache, "kv_cache", torch.uint8, dev)
+    _check(slots, "slots", torch.int64, dev)
+    M = slots.numel()
+    if out is None:
+        out = torch.empty((M, HEAD_DIM), dtype=dtype, device=dev)
+    _check(out, "out", dtype, dev)
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        st = kvc_dequantize(kv_cache.data_ptr(), kv_cache.shape[0], slots.data_ptr(), M,
+                            out.data_ptr(),
+                            KVC_DTYPE_BF16 if dtype == torch.bfloat16 else KVC_DTYPE_F32,
+                            int(s.cuda_stream))
+    if st != KVC_OK:
+        raise KvcError(st, "kvc_dequantize")
+    return out
 
 
 # ---- torch-facing wrapper with the statement's signature ----------------------

@@ -249,6 +249,24 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
   return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
+kvc_status kvc_dequantize(const uint8_t* kv_cache, int64_t num_kv_pages, const int64_t* slots,
+                          int64_t num_slots, void* out, int32_t out_dtype, void* stream) {
+  if (num_slots < 0 || (out_dtype != KVC_DTYPE_F32 && out_dtype != KVC_DTYPE_BF16))
+    return KVC_ERR_INVALID_ARG;
+  if (num_slots == 0) return KVC_OK;
+  if (!kv_cache || !slots || !out || num_kv_pages <= 0) return KVC_ERR_INVALID_ARG;
+  if (!aligned(kv_cache, 16) || !aligned(slots, 8) ||
+      !aligned(out, out_dtype == KVC_DTYPE_F32 ? 16 : 8))
+    return KVC_ERR_INVALID_ARG;
+  DeviceInfo d;
+  const kvc_status st = device_info(&d);
+  if (st != KVC_OK) return st;
+  const cudaError_t e = kvc::launch_dequantize(kv_cache, num_kv_pages, slots, num_slots, out,
+                                               out_dtype == KVC_DTYPE_BF16, d.error_word,
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
 kvc_status kvc_get_device_error(void* stream, uint32_t* out_code) {
   if (out_code == nullptr) return KVC_ERR_INVALID_ARG;
   DeviceInfo d;

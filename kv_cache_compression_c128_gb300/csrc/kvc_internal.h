@@ -86,4 +86,9 @@ size_t cluster_smem_bytes(int cluster_size);
 int cluster_capacity(int cluster_size);  // sets the kernel up; co-resident clusters (0: refused)
 cudaError_t launch_cluster(const Params& p, int clusters, cudaStream_t stream);
 
+// reader direction (kvc_reader.cu)
+cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_t* slots,
+                              int64_t num_slots, void* out, int out_bf16, uint32_t* err,
+                              cudaStream_t stream);
+
 }  // namespace kvc

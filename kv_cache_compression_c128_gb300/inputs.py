@@ -223,6 +223,15 @@ def ragged_case(compress_ratio: int = 128, total_tokens: int = 131072,
                      lengths=L, name=f"ragged_r{num_reqs}_t{total_tokens}_c{compress_ratio}")
 
 
+def general_window_case(compress_ratio: int = 128, block_size: int = 16) -> Case:
+    """Headline-sized call with general windows: 8 requests x 16384 tokens,
+    block_size 16, 128 windows per request at random starts (1024 outputs)."""
+    seed = BASE_SEED + 300 + compress_ratio + block_size
+    return make_case(8, 131072, compress_ratio, seed=seed, block_size=block_size,
+                     boundaries_per_req=128,
+                     name=f"general_r8_t131072_c{compress_ratio}_b{block_size}")
+
+
 def headline_case() -> Case:
     """8 requests x 16384 tokens, compress_ratio 128: the largest case."""
     return bench_case(BENCH_SHAPES.index((8, 131072, 128)))

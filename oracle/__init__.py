@@ -76,6 +76,8 @@ def _load():
                 P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P,
                 I64, I32, I32, F32, P, P, P]
             lib.kvc_oracle_compress.restype = ctypes.c_int
+            lib.kvc_oracle_dequantize.argtypes = [P, I64, P, I64, P, I32]
+            lib.kvc_oracle_dequantize.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -198,6 +200,17 @@ def compress(state_bits, token_to_req, positions, boundary_token_indices,
         _ptr(sm), sm.shape[0], _ptr(kv_cache), kv_cache.shape[0], block_size,
         compress_ratio, float(rms_norm_eps), _ptr(c), _ptr(y), _ptr(valid))
     return {"c": c, "y": y, "valid": valid, "status": int(status)}
+
+
+def dequantize(kv_cache, slots, out_bf16: bool = False):
+    """Decode slots back to vectors: float32 [M, 512], or raw bf16 bits
+    (uint16 [M, 512]) when out_bf16.  Returns (out, status)."""
+    assert kv_cache.flags.c_contiguous and kv_cache.dtype == np.uint8
+    sl = _c(slots, np.int64)
+    out = np.zeros((sl.shape[0], HEAD_DIM), dtype=np.uint16 if out_bf16 else np.float32)
+    st = _load().kvc_oracle_dequantize(_ptr(kv_cache), kv_cache.shape[0], _ptr(sl),
+                                       sl.shape[0], _ptr(out), 1 if out_bf16 else 0)
+    return out, int(st)
 
 
 def compress_case(case, kv_cache=None):

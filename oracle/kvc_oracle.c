@@ -22,6 +22,9 @@
  * quantisation, RoPE) is evaluated in fp32 exactly as the page's finalizer
  * does, one rounded operation at a time; build with -ffp-contract=off.
  *
+ * The reader direction (kvc_oracle_dequantize) decodes a packed slot back to
+ * a 512-vector: NOPE values q * 2^(scale - 127), RoPE values as stored.
+ *
  * Parity pins: every function here is pinned by tests/test_oracle_*.py
  * against closed forms, library routines (torch softmax / rms_norm / bf16
  * cast, complex multiplication), exact rational arithmetic and hand-worked
@@ -309,4 +312,49 @@ int kvc_oracle_compress(
       compress_ratio, cos_sin_cache, num_positions, kv_slot_mapping,
       slot_mapping_len, kv_cache, num_kv_pages);
   return st1 != OR_OK ? st1 : st2;
+}
+
+/*
+ * Read slots back ("Gather and Scatter" layout; the values the quantisation
+ * equation of "How One Output Is Produced" encodes): for each slot m,
+ *   out[m, d] = q_d * 2^(scale[d / 64] - 127)   for d < 448 (q_d the int8 code),
+ *   out[m, d] = the stored bf16 RoPE value       for d >= 448,
+ * written as float (out_bf16 == 0, `out` is float [M, 512]) or as bf16 bits
+ * (out_bf16 != 0, `out` is uint16 [M, 512], float value rounded to nearest
+ * even).  q * 2^e is evaluated exactly in double before the single rounding.
+ * A negative slot yields zeros; a slot beyond the last page yields zeros and
+ * OR_BAD_INDEX.
+ */
+int kvc_oracle_dequantize(const uint8_t* kv_cache, int64_t num_kv_pages,
+                          const int64_t* slots, int64_t num_slots, void* out,
+                          int32_t out_bf16) {
+  int status = OR_OK;
+  for (int64_t m = 0; m < num_slots; ++m) {
+    float vals[OR_HEAD_DIM];
+    for (int d = 0; d < OR_HEAD_DIM; ++d) vals[d] = 0.0f;
+    int64_t slot = slots[m];
+    int64_t page = slot / OR_SLOTS_PER_PAGE, off = slot % OR_SLOTS_PER_PAGE;
+    if (slot >= 0 && page >= num_kv_pages) status = OR_BAD_INDEX;
+    if (slot >= 0 && page < num_kv_pages) {
+      const uint8_t* pg = kv_cache + page * (int64_t)OR_PAGE_BYTES;
+      const uint8_t* payload = pg + off * OR_TOKEN_STRIDE;
+      const uint8_t* scale = pg + OR_SLOTS_PER_PAGE * OR_TOKEN_STRIDE + off * OR_SCALE_DIM;
+      for (int d = 0; d < OR_NOPE_DIM; ++d) {
+        int q = (int)(int8_t)payload[d];
+        int e = (int)scale[d / OR_GROUP] - 127;
+        vals[d] = (float)ldexp((double)q, e);
+      }
+      for (int j = 0; j < OR_ROPE_DIM; ++j) {
+        const uint8_t* b = payload + OR_NOPE_DIM + 2 * j;
+        vals[OR_NOPE_DIM + j] = or_bf16_bits_to_float((uint16_t)(b[0] | (b[1] << 8)));
+      }
+    }
+    for (int d = 0; d < OR_HEAD_DIM; ++d) {
+      if (out_bf16)
+        ((uint16_t*)out)[m * OR_HEAD_DIM + d] = kvc_oracle_f32_to_bf16(vals[d]);
+      else
+        ((float*)out)[m * OR_HEAD_DIM + d] = vals[d];
+    }
+  }
+  return status;
 }

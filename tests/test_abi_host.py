@@ -127,3 +127,22 @@ def test_torch_wrapper_rejects_cpu_tensors(kvc):
                                   t(case.boundary_token_indices), t(case.block_table),
                                   t(case.rms_norm_weight), t(case.cos_sin_cache),
                                   t(case.kv_slot_mapping), t(case.kv_cache), 8, 16)
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(out_dtype=7), 1),
+    (dict(num_slots=-1), 1),
+    (dict(kv_cache=0), 1),
+    (dict(out=0x30004), 1),            # fp32 output must be 16-byte aligned
+    (dict(slots=0x20004), 1),
+    (dict(num_kv_pages=0), 1),
+])
+def test_dequantize_host_validation(kvc, change, status):
+    args = dict(kv_cache=0x10000, num_kv_pages=1, slots=0x20000, num_slots=8, out=0x30000,
+                out_dtype=0, stream=0)
+    args.update(change)
+    assert kvc.kvc_dequantize(**args) == status
+
+
+def test_dequantize_zero_slots_is_a_no_op(kvc):
+    assert kvc.kvc_dequantize(0x10000, 1, 0x20000, 0, 0x30000, 0, 0) == 0

@@ -155,3 +155,60 @@ def test_negative_slot_is_skipped_and_slot_mapping_by_output(oracle_mod):
     m = written_mask(kv_skip.shape, [old])
     assert np.array_equal(kv_skip.reshape(-1)[m], case.kv_cache.reshape(-1)[m])
     assert np.array_equal(kv_skip.reshape(-1)[~m], kv_tok.reshape(-1)[~m])
+
+
+# ---- the reader direction: decode packed slots back to vectors -----------------
+
+def test_dequantize_hand_worked_golden_slots(oracle_mod):
+    # the two hand-worked slots decode to the hand-derived values:
+    # group g has e = g - 9, so a code q reads back as q * 2^(g - 9); RoPE +-1
+    with open(os.path.join(GOLDEN, "hand_worked_two_slots.json")) as f:
+        spec = json.load(f)
+    arrays, vA, vB = _hand_worked_inputs()
+    kv = np.full((1, 37376), 0xAB, np.uint8)
+    oracle_mod.compress(kv_cache=kv, **arrays)
+    out, st = oracle_mod.dequantize(kv, np.array([1, 0, -1], np.int64))
+    assert st == 0
+    code = spec["expected"]["code_by_j"]
+    for row, v in ((0, vA), (1, vB)):
+        for d in range(448):
+            q = code.get(str(d % 64), code["other"]) * (1 if v[d] > 0 else -1)
+            assert out[row, d] == q * 2.0 ** (d // 64 - 9)
+    assert np.all(np.abs(out[0, 448:]) == 1.0) and np.all(np.abs(out[1, 448:]) == 1.0)
+    assert np.array_equal(np.sign(out[0, 448:]), np.sign(vA[448:]))
+    assert np.all(out[2] == 0.0)                  # negative slot: zeros
+
+
+def test_dequantize_edge_bytes(oracle_mod):
+    kv = np.zeros((1, 37376), np.uint8)
+    pay = kv[0, 0:576]
+    sc = kv[0, 36864:36872]
+    pay[0], sc[0] = 0x81, 127                     # -127 * 2^0
+    pay[64], pay[65], sc[1] = 0x01, 0x00, 0       # 2^-127 (subnormal), 0
+    pay[128], pay[129], sc[2] = 0x01, 0x00, 255   # 2^128 -> inf, 0 * 2^128 -> 0
+    pay[448], pay[449] = 0x80, 0xBF               # bf16 0xBF80 = -1.0
+    out, st = oracle_mod.dequantize(kv, np.array([0], np.int64))
+    assert st == 0
+    assert out[0, 0] == -127.0
+    assert out[0, 64] == np.float32(2.0 ** -127) and out[0, 65] == 0.0
+    assert np.isinf(out[0, 128]) and out[0, 128] > 0 and out[0, 129] == 0.0
+    assert out[0, 448] == -1.0
+    bits, _ = oracle_mod.dequantize(kv, np.array([0], np.int64), out_bf16=True)
+    assert bits[0, 0] == 0xC2FE                   # -127 in bf16
+    assert bits[0, 128] == 0x7F80 and bits[0, 448] == 0xBF80
+    _, st = oracle_mod.dequantize(kv, np.array([64], np.int64))
+    assert st == 4                                # slot beyond the last page
+
+
+def test_dequantize_matches_bit_level_decoder(oracle_mod):
+    # random bytes everywhere (codes and scale exponents over their full
+    # range): the oracle's reader equals the tests' own byte decoder
+    rng = np.random.default_rng(40)
+    kv = rng.integers(0, 256, size=(2, 37376), dtype=np.uint8)
+    slots = rng.permutation(128)[:50]
+    out, st = oracle_mod.dequantize(kv, slots)
+    assert st == 0
+    for m, s in enumerate(slots):
+        q, e, _, rope = decode_slot(kv, s)
+        want = np.concatenate([dequant(q, e), rope.astype(np.float64)]).astype(np.float32)
+        assert np.array_equal(out[m], want, equal_nan=True)
