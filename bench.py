@@ -299,6 +299,55 @@ def time_reader(kvc, case, device, steps: int = 2000):
     return {"slots": M, **res}
 
 
+def time_layers(kvc, case, device, L: int = 8, steps: int = 1000):
+    """Per-call time of kvc_compress_layers over L layers of `case` (each
+    layer its own state copy, weight and kv_cache; >= 3 rotating sets so the
+    L * state bytes are not served from L2), against the per-call time of the
+    single-layer call on the same shape."""
+    import torch
+
+    sets = max(3, -(-ROTATE_MIN_BYTES // (L * case.state_bits.nbytes)))
+    states0, d = _tensors(case, device, 1)
+    states = [[states0[0].clone() for _ in range(L)] for _ in range(sets)]
+    weights = [d["rms_norm_weight"].clone() for _ in range(L)]
+    kvs = [d["kv_cache"].clone() for _ in range(L)]
+    ws = torch.zeros(kvc.kvc_workspace_bytes(case.num_outputs), dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def call(i):
+        kvc.compress_layers(states[i % sets], d["token_to_req"], d["positions"],
+                            d["boundary_token_indices"], d["block_table"], weights,
+                            d["cos_sin_cache"], d["kv_slot_mapping"], kvs, case.block_size,
+                            case.compress_ratio, case.rms_norm_eps, stream=stream, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            call(i)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        chunk = 100
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(chunk):
+                call(i)
+        g.replay()
+        torch.cuda.synchronize(device)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(1, steps // chunk)
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+    assert kvc.kvc_get_device_error(stream.cuda_stream) == 0
+    t = ev0.elapsed_time(ev1) / 1e3 / (reps * chunk)
+    b = L * bytes_for(case)
+    single, _ = time_device(kvc, case, device, 1000, 20)
+    return {"shape": case.name, "layers": L, "us_per_call": round(t * 1e6, 3),
+            "gb_s": round(b / t / 1e9, 1), "us_per_layer": round(t * 1e6 / L, 3),
+            "single_layer_us_per_call": round(single * 1e6, 3),
+            "speedup_vs_single_calls": round(L * single / t, 2)}
+
+
 def time_e2e(kvc, case, device, steps: int, warmup: int):
     """Seconds per call through the public API from pinned host buffers:
     H2D of every input, the call, D2H of kv_cache, all inside the region."""
@@ -432,6 +481,7 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     reader = time_reader(kvc, case, device) if rank == 0 else None
+    layers = time_layers(kvc, inputs.bench_case(0), device, 8) if rank == 0 else None
 
     sweep = None
     if not args.no_sweep and rank == 0:
@@ -493,6 +543,7 @@ def main():
         "clocks": clocks,
         "e2e": e2e,
         "reader": reader,
+        "layers": layers,
         "cpu_baseline": cpu,
         "sweep": sweep,
         "kernel_source_hash": kernel_source_hash(),

@@ -125,6 +125,35 @@ kvc_status kvc_compress(
     float* y_out, void* workspace, size_t workspace_bytes,
     uint32_t flags, void* stream);
 
+/*
+ * kvc_compress for num_layers layers (1..64) that share every index array:
+ * the same boundary tokens, windows, block table, slots, cos/sin table and
+ * eps, each layer with its own state cache, RMSNorm weight and kv_cache
+ * (per-layer caches of a model: the write-up's motivation is long-context
+ * decoding, where every layer compresses the same windows).  One launch
+ * serves all layers: the index chain is resolved per window and the work of
+ * all layers is split evenly over the GPU.
+ *
+ * state_caches, rms_norm_weights, kv_caches: HOST arrays of num_layers
+ * DEVICE pointers, each with the shape, alignment and meaning of the single
+ * buffer of kvc_compress.  y_out (optional): fp32 [num_layers * num_outputs,
+ * 512], layer-major.  workspace: kvc_workspace_bytes(num_outputs) bytes
+ * (the stream-K route processes one layer at a time).  Everything else as for
+ * kvc_compress, whose results each layer reproduces.
+ */
+kvc_status kvc_compress_layers(
+    int32_t num_layers, const void* const* state_caches, int64_t num_state_blocks,
+    const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
+    const int64_t* boundary_token_indices, int64_t num_outputs,
+    const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    const float* const* rms_norm_weights,
+    const float* cos_sin_cache, int64_t num_positions,
+    const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+    uint8_t* const* kv_caches, int64_t num_kv_pages,
+    int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
+    float* y_out, void* workspace, size_t workspace_bytes,
+    uint32_t flags, void* stream);
+
 /* Output element types of kvc_dequantize. */
 #define KVC_DTYPE_F32 0
 #define KVC_DTYPE_BF16 1

@@ -136,6 +136,10 @@ def lib():
                 P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P, I64,
                 I32, I32, ctypes.c_float, P, U32, P]
             L.kvc_compress_static.restype = ctypes.c_int
+            L.kvc_compress_layers.argtypes = [
+                I32, P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P, I64,
+                I32, I32, ctypes.c_float, P, P, ctypes.c_size_t, U32, P]
+            L.kvc_compress_layers.restype = ctypes.c_int
             L.kvc_dequantize.argtypes = [P, I64, P, I64, P, I32, P]
             L.kvc_dequantize.restype = ctypes.c_int
             L.kvc_query_launch.argtypes = [I64, I32, U32, P, P, P, P]
@@ -218,6 +222,25 @@ def kvc_compress_static(state_cache, num_state_blocks, token_to_req, positions, 
         max_blocks_per_req, v(rms_norm_weight), v(cos_sin_cache), num_positions,
         v(kv_slot_mapping), slot_mapping_len, v(kv_cache), num_kv_pages, block_size,
         compress_ratio, ctypes.c_float(rms_norm_eps), v(y_out), flags, v(stream)))
+
+
+def kvc_compress_layers(num_layers, state_caches, num_state_blocks, token_to_req, positions,
+                        num_tokens, boundary_token_indices, num_outputs, block_table, num_reqs,
+                        max_blocks_per_req, rms_norm_weights, cos_sin_cache, num_positions,
+                        kv_slot_mapping, slot_mapping_len, kv_caches, num_kv_pages, block_size,
+                        compress_ratio, rms_norm_eps, y_out, workspace, workspace_bytes, flags,
+                        stream) -> int:
+    """The multi-layer entry point; the three per-layer arguments are
+    sequences of integer device pointers.  Returns the status."""
+    v = ctypes.c_void_p
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*[int(x) for x in xs])
+    return int(lib().kvc_compress_layers(
+        int(num_layers), arr(state_caches), num_state_blocks, v(token_to_req), v(positions),
+        num_tokens, v(boundary_token_indices), num_outputs, v(block_table), num_reqs,
+        max_blocks_per_req, arr(rms_norm_weights), v(cos_sin_cache), num_positions,
+        v(kv_slot_mapping), slot_mapping_len, arr(kv_caches), num_kv_pages, block_size,
+        compress_ratio, ctypes.c_float(rms_norm_eps), v(y_out), v(workspace), workspace_bytes,
+        flags, v(stream)))
 
 
 def kvc_dequantize(kv_cache, num_kv_pages, slots, num_slots, out, out_dtype, stream) -> int:
@@ -348,3 +371,54 @@ def c128_256_512_compress(state_cache, token_to_req, positions, boundary_token_i
     if st != KVC_OK:
         raise KvcError(st, "kvc_compress")
     return kv_cache
+
+
+def compress_layers(state_caches, token_to_req, positions, boundary_token_indices, block_table,
+                    rms_norm_weights, cos_sin_cache, kv_slot_mapping, kv_caches, block_size,
+                    compress_ratio, rms_norm_eps=1.0e-6, *, y_out=None, flags: int = 0,
+                    stream=None, workspace=None):
+    """c128_256_512_compress for several layers in one launch: lists of
+    per-layer state caches, RMSNorm weights and kv caches (same shapes and
+    dtypes as the single-layer call) sharing every index array.  y_out, if
+    given, is fp32 [L * N, 512] (layer-major).  Returns kv_caches."""
+    import torch
+
+    L = len(state_caches)
+    if not (len(rms_norm_weights) == L == len(kv_caches)) or L < 1:
+        raise ValueError("state_caches, rms_norm_weights and kv_caches need one entry per layer")
+    dev = state_caches[0].device
+    if dev.type != "cuda":
+        raise ValueError("state caches must be CUDA tensors (there is no CPU path)")
+    for l in range(L):
+        _check(state_caches[l], f"state_caches[{l}]", torch.bfloat16, dev)
+        _check(rms_norm_weights[l], f"rms_norm_weights[{l}]", torch.float32, dev)
+        _check(kv_caches[l], f"kv_caches[{l}]", torch.uint8, dev)
+        if state_caches[l].shape != state_caches[0].shape or kv_caches[l].shape != kv_caches[0].shape:
+            raise ValueError("all layers need the same state and kv_cache shapes")
+    for name, t, dt in (("token_to_req", token_to_req, torch.int32), ("positions", positions, torch.int64),
+                        ("boundary_token_indices", boundary_token_indices, torch.int64),
+                        ("block_table", block_table, torch.int32),
+                        ("cos_sin_cache", cos_sin_cache, torch.float32),
+                        ("kv_slot_mapping", kv_slot_mapping, torch.int64)):
+        _check(t, name, dt, dev)
+    N = boundary_token_indices.numel()
+    if y_out is not None:
+        _check(y_out, "y_out", torch.float32, dev)
+        if y_out.numel() < L * N * HEAD_DIM:
+            raise ValueError("y_out must hold num_layers * num_outputs * 512 floats")
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        sp = int(s.cuda_stream)
+        ws = workspace if workspace is not None else workspace_for(dev, sp, N)
+        st = kvc_compress_layers(
+            L, [t.data_ptr() for t in state_caches], state_caches[0].shape[0],
+            token_to_req.data_ptr(), positions.data_ptr(), positions.numel(),
+            boundary_token_indices.data_ptr(), N, block_table.data_ptr(), block_table.shape[0],
+            block_table.shape[1], [t.data_ptr() for t in rms_norm_weights],
+            cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], kv_slot_mapping.data_ptr(),
+            kv_slot_mapping.numel(), [t.data_ptr() for t in kv_caches], kv_caches[0].shape[0],
+            int(block_size), int(compress_ratio), float(rms_norm_eps),
+            0 if y_out is None else y_out.data_ptr(), ws.data_ptr(), ws.numel(), int(flags), sp)
+    if st != KVC_OK:
+        raise KvcError(st, "kvc_compress_layers")
+    return kv_caches

@@ -174,6 +174,112 @@ kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio, uint32_
   return KVC_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// kvc_compress for L layers that share every index array: host arrays of L
+// device pointers for the state caches, weights and kv caches.
+kvc_status compress_layers(int32_t L, const void* const* state_caches, int64_t num_state_blocks,
+                           const int32_t* token_to_req, const int64_t* positions,
+                           int64_t num_tokens, const int64_t* boundary_token_indices,
+                           int64_t num_outputs, const int32_t* block_table, int64_t num_reqs,
+                           int64_t max_blocks_per_req, const float* const* rms_norm_weights,
+                           const float* cos_sin_cache, int64_t num_positions,
+                           const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+                           uint8_t* const* kv_caches, int64_t num_kv_pages, int32_t block_size,
+                           int32_t compress_ratio, float rms_norm_eps, float* y_out,
+                           void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+  if (num_outputs < 0 || (flags & ~KVC_FLAG_ALL) != 0) return KVC_ERR_INVALID_ARG;
+  if (L < 1 || L > kvc::kMaxLayers) return KVC_ERR_INVALID_ARG;
+  if (block_size < kvc::kBlockRows) return KVC_ERR_UNSUPPORTED;
+  if (compress_ratio <= 0) return KVC_ERR_INVALID_ARG;
+  if (!std::isfinite(rms_norm_eps) || rms_norm_eps < 0.f) return KVC_ERR_INVALID_ARG;
+  if (num_outputs == 0) return KVC_OK;
+  if (!state_caches || !rms_norm_weights || !kv_caches) return KVC_ERR_INVALID_ARG;
+  for (int l = 0; l < L; ++l) {
+    if (!state_caches[l] || !rms_norm_weights[l] || !kv_caches[l]) return KVC_ERR_INVALID_ARG;
+    if (!aligned(state_caches[l], 16) || !aligned(kv_caches[l], 16) ||
+        !aligned(rms_norm_weights[l], 8))
+      return KVC_ERR_INVALID_ARG;
+  }
+  if (!token_to_req || !positions || !boundary_token_indices || !block_table || !cos_sin_cache ||
+      !kv_slot_mapping || !workspace)
+    return KVC_ERR_INVALID_ARG;
+  if (num_state_blocks <= 0 || num_tokens <= 0 || num_reqs <= 0 || max_blocks_per_req <= 0 ||
+      num_positions <= 0 || num_kv_pages <= 0)
+    return KVC_ERR_INVALID_ARG;
+  if (slot_mapping_len != num_tokens && slot_mapping_len != num_outputs) return KVC_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16) || (y_out && !aligned(y_out, 8)) || !aligned(token_to_req, 4) ||
+      !aligned(block_table, 4) || !aligned(cos_sin_cache, 4) || !aligned(positions, 8) ||
+      !aligned(boundary_token_indices, 8) || !aligned(kv_slot_mapping, 8))
+    return KVC_ERR_INVALID_ARG;
+
+  DeviceInfo d;
+  const kvc_status st = device_info(&d);
+  if (st != KVC_OK) return st;
+  const int max_ctas = d.sms * d.streamk_ctas_per_sm;
+  const kvc::WorkspaceLayout WL = kvc::workspace_layout(max_ctas, num_outputs);
+  if (workspace_bytes < WL.total) return KVC_ERR_INVALID_ARG;
+
+  kvc::Params p = {};
+  for (int l = 0; l < L; ++l) {
+    p.states[l] = static_cast<const uint16_t*>(state_caches[l]);
+    p.weights[l] = rms_norm_weights[l];
+    p.kvs[l] = kv_caches[l];
+  }
+  p.num_layers = L;
+  p.num_blocks = num_state_blocks;
+  p.token_to_req = token_to_req;
+  p.positions = positions;
+  p.num_tokens = num_tokens;
+  p.bti = boundary_token_indices;
+  p.num_outputs = num_outputs;
+  p.block_table = block_table;
+  p.num_reqs = num_reqs;
+  p.max_blocks = max_blocks_per_req;
+  p.cos_sin = cos_sin_cache;
+  p.num_positions = num_positions;
+  p.slot_map = kv_slot_mapping;
+  p.slot_by_token = (slot_mapping_len == num_tokens) ? 1 : 0;
+  p.num_pages = num_kv_pages;
+  p.y_out = y_out;
+  p.compress_ratio = compress_ratio;
+  p.block_size = block_size;
+  p.blocks_per_output = (compress_ratio + kvc::kBlockRows - 1) / kvc::kBlockRows;
+  p.num_units = num_outputs * p.blocks_per_output;
+  p.eps = rms_norm_eps;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.partials = reinterpret_cast<float*>(ws + WL.partials);
+  p.part_status = reinterpret_cast<int32_t*>(ws + WL.status);
+  p.counters = reinterpret_cast<int32_t*>(ws + WL.counters);
+  p.error = d.error_word;
+
+  const bool aligned8 = block_size == kvc::kBlockRows && compress_ratio % kvc::kBlockRows == 0;
+  Route r;
+  if (!pick_route(d, num_outputs * L, p.blocks_per_output, aligned8, flags, &r))
+    return KVC_ERR_UNSUPPORTED;
+  p.cluster_size = r.cluster;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!r.stream_k) return kvc::launch_cluster(p, r.count, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+  // stream-K: one launch per layer (each reuses the workspace, in stream order)
+  const int ctas = pick_route(d, num_outputs, p.blocks_per_output, aligned8, flags, &r) ? r.count : 1;
+  for (int l = 0; l < L; ++l) {
+    kvc::Params pl = p;
+    pl.states[0] = p.states[l];
+    pl.weights[0] = p.weights[l];
+    pl.kvs[0] = p.kvs[l];
+    pl.num_layers = 1;
+    pl.y_out = y_out ? y_out + static_cast<int64_t>(l) * num_outputs * kvc::kHeadDim : nullptr;
+    if (kvc::launch_streamk(pl, ctas, s) != cudaSuccess) return KVC_ERR_CUDA;
+  }
+  return KVC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
                         const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
                         const int64_t* boundary_token_indices, int64_t num_outputs,
@@ -184,69 +290,32 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
                         int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
                         float* y_out, void* workspace, size_t workspace_bytes, uint32_t flags,
                         void* stream) {
-  if (num_outputs < 0 || (flags & ~KVC_FLAG_ALL) != 0) return KVC_ERR_INVALID_ARG;
-  if (block_size < kvc::kBlockRows) return KVC_ERR_UNSUPPORTED;
-  if (compress_ratio <= 0) return KVC_ERR_INVALID_ARG;
-  if (!std::isfinite(rms_norm_eps) || rms_norm_eps < 0.f) return KVC_ERR_INVALID_ARG;
-  if (num_outputs == 0) return KVC_OK;
-  if (!state_cache || !token_to_req || !positions || !boundary_token_indices || !block_table ||
-      !rms_norm_weight || !cos_sin_cache || !kv_slot_mapping || !kv_cache || !workspace)
-    return KVC_ERR_INVALID_ARG;
-  if (num_state_blocks <= 0 || num_tokens <= 0 || num_reqs <= 0 || max_blocks_per_req <= 0 ||
-      num_positions <= 0 || num_kv_pages <= 0)
-    return KVC_ERR_INVALID_ARG;
-  if (slot_mapping_len != num_tokens && slot_mapping_len != num_outputs) return KVC_ERR_INVALID_ARG;
-  if (!aligned(state_cache, 16) || !aligned(kv_cache, 16) || !aligned(workspace, 16) ||
-      !aligned(rms_norm_weight, 8) || (y_out && !aligned(y_out, 8)) ||
-      !aligned(token_to_req, 4) || !aligned(block_table, 4) || !aligned(cos_sin_cache, 4) ||
-      !aligned(positions, 8) || !aligned(boundary_token_indices, 8) || !aligned(kv_slot_mapping, 8))
-    return KVC_ERR_INVALID_ARG;
+  return compress_layers(1, &state_cache, num_state_blocks, token_to_req, positions, num_tokens,
+                         boundary_token_indices, num_outputs, block_table, num_reqs,
+                         max_blocks_per_req, &rms_norm_weight, cos_sin_cache, num_positions,
+                         kv_slot_mapping, slot_mapping_len, &kv_cache, num_kv_pages, block_size,
+                         compress_ratio, rms_norm_eps, y_out, workspace, workspace_bytes, flags,
+                         stream);
+}
 
-  DeviceInfo d;
-  const kvc_status st = device_info(&d);
-  if (st != KVC_OK) return st;
-  const int max_ctas = d.sms * d.streamk_ctas_per_sm;
-  const kvc::WorkspaceLayout L = kvc::workspace_layout(max_ctas, num_outputs);
-  if (workspace_bytes < L.total) return KVC_ERR_INVALID_ARG;
-
-  kvc::Params p;
-  p.state = static_cast<const uint16_t*>(state_cache);
-  p.num_blocks = num_state_blocks;
-  p.token_to_req = token_to_req;
-  p.positions = positions;
-  p.num_tokens = num_tokens;
-  p.bti = boundary_token_indices;
-  p.num_outputs = num_outputs;
-  p.block_table = block_table;
-  p.num_reqs = num_reqs;
-  p.max_blocks = max_blocks_per_req;
-  p.weight = rms_norm_weight;
-  p.cos_sin = cos_sin_cache;
-  p.num_positions = num_positions;
-  p.slot_map = kv_slot_mapping;
-  p.slot_by_token = (slot_mapping_len == num_tokens) ? 1 : 0;
-  p.kv = kv_cache;
-  p.num_pages = num_kv_pages;
-  p.y_out = y_out;
-  p.compress_ratio = compress_ratio;
-  p.block_size = block_size;
-  p.blocks_per_output = (compress_ratio + kvc::kBlockRows - 1) / kvc::kBlockRows;
-  p.num_units = num_outputs * p.blocks_per_output;
-  p.eps = rms_norm_eps;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.partials = reinterpret_cast<float*>(ws + L.partials);
-  p.part_status = reinterpret_cast<int32_t*>(ws + L.status);
-  p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
-  p.error = d.error_word;
-
-  Route r;
-  const bool aligned = block_size == kvc::kBlockRows && compress_ratio % kvc::kBlockRows == 0;
-  if (!pick_route(d, num_outputs, p.blocks_per_output, aligned, flags, &r)) return KVC_ERR_UNSUPPORTED;
-  p.cluster_size = r.cluster;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e =
-      r.stream_k ? kvc::launch_streamk(p, r.count, s) : kvc::launch_cluster(p, r.count, s);
-  return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+kvc_status kvc_compress_layers(int32_t num_layers, const void* const* state_caches,
+                               int64_t num_state_blocks, const int32_t* token_to_req,
+                               const int64_t* positions, int64_t num_tokens,
+                               const int64_t* boundary_token_indices, int64_t num_outputs,
+                               const int32_t* block_table, int64_t num_reqs,
+                               int64_t max_blocks_per_req, const float* const* rms_norm_weights,
+                               const float* cos_sin_cache, int64_t num_positions,
+                               const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+                               uint8_t* const* kv_caches, int64_t num_kv_pages, int32_t block_size,
+                               int32_t compress_ratio, float rms_norm_eps, float* y_out,
+                               void* workspace, size_t workspace_bytes, uint32_t flags,
+                               void* stream) {
+  return compress_layers(num_layers, state_caches, num_state_blocks, token_to_req, positions,
+                         num_tokens, boundary_token_indices, num_outputs, block_table, num_reqs,
+                         max_blocks_per_req, rms_norm_weights, cos_sin_cache, num_positions,
+                         kv_slot_mapping, slot_mapping_len, kv_caches, num_kv_pages, block_size,
+                         compress_ratio, rms_norm_eps, y_out, workspace, workspace_bytes, flags,
+                         stream);
 }
 
 kvc_status kvc_dequantize(const uint8_t* kv_cache, int64_t num_kv_pages, const int64_t* slots,

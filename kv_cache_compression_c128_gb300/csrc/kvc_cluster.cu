@@ -13,7 +13,10 @@
 // 8).  Output n is handled by one thread-block cluster of S CTAs (S = 1, 2,
 // 4, 8, 16); rank j streams chunks [j K/S, (j+1) K/S).  Persistent clusters
 // take contiguous, equal ranges of outputs, so every CTA streams the same
-// number of chunks.
+// number of chunks.  A multi-layer call simply has L * N outputs: output o is
+// window o mod N of layer o / N (same chunks, that layer's state cache,
+// weight and kv_cache), so all layers share one launch and one balanced
+// split.
 //
 // Inside a CTA (320 threads):
 //   warp 9  resolver: turns units into physical blocks (boundary index ->
@@ -55,6 +58,8 @@ struct alignas(16) FifoEntry {
   int n1, n2;            // rows in each run
   int first;             // first unit of its output in this CTA
   int piece;             // output index relative to the cluster's first output
+  int layer;             // layer whose state cache the chunk is read from
+  int pad_;
 };
 
 template <int S>
@@ -89,13 +94,16 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int6
   const int lane = threadIdx.x & 31;
   for (int64_t c = 0; c * kFifoChunk < units; ++c) {
     const int64_t i = c * kFifoChunk + lane;
-    FifoEntry e{-1, -1, -1, -1, 0, 0, 0, 0};
+    FifoEntry e{-1, -1, -1, -1, 0, 0, 0, 0, 0, 0};
     if (i < units) {
       const int64_t q = i / kj;
       const int kk = static_cast<int>(i - q * kj);
+      const int64_t o = n0 + q;                       // output of the L * N space
+      const int layer = static_cast<int>(o / p.num_outputs);
       MetaRec rec;
       ChunkRuns cr;
-      resolve_chunk(p, n0 + q, k_lo + kk, kk == 0, cr, rec);
+      resolve_chunk(p, o - static_cast<int64_t>(layer) * p.num_outputs, k_lo + kk, kk == 0, cr, rec);
+      e.layer = layer;
       e.row1 = cr.row1;
       e.row2 = cr.row2;
       e.n1 = cr.n1;
@@ -162,9 +170,10 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
         uint8_t* dst = ring + static_cast<size_t>(stage) * kBlockBytes;
         sh.stage_rows[stage] = static_cast<uint32_t>(e.n1 + e.n2);
         mbar_arrive_expect_tx(&sh.full_bar[stage], (e.n1 + e.n2) * kRowBytes);
-        bulk_copy_g2s(dst, p.state + e.row1 * kRowElems, e.n1 * kRowBytes, &sh.full_bar[stage], policy);
+        const uint16_t* state = p.states[e.layer];
+        bulk_copy_g2s(dst, state + e.row1 * kRowElems, e.n1 * kRowBytes, &sh.full_bar[stage], policy);
         if (e.n2 > 0)
-          bulk_copy_g2s(dst + e.n1 * kRowBytes, p.state + e.row2 * kRowElems, e.n2 * kRowBytes,
+          bulk_copy_g2s(dst + e.n1 * kRowBytes, state + e.row2 * kRowElems, e.n2 * kRowBytes,
                         &sh.full_bar[stage], policy);
       } else {
         sh.stage_rows[stage] = 0;
@@ -202,7 +211,8 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
   int stage = 0;
   uint32_t phase = 0, mph = 0;
   for (int64_t q = 0; q < n1 - n0; ++q) {
-    const int64_t n = n0 + q;
+    const int64_t o = n0 + q;  // output row of the L * N space
+    const int layer = static_cast<int>(o / p.num_outputs);
     SoftmaxState s;
     state_reset(s);
     bool bad = false;
@@ -240,7 +250,7 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
     if constexpr (S == 1) {
       const float c0 = s.a0 / s.d0, c1 = s.a1 / s.d1;
       const float total = consumer_sum_squares(sh.fs, c0, c1);
-      finalize_slice(p, sh.fs, n, true, 2 * t, c0, c1, bad, meta, cs, sn, total, 0, kHeadDim);
+      finalize_slice(p, sh.fs, layer, o, true, 2 * t, c0, c1, bad, meta, cs, sn, total, 0, kHeadDim);
     } else {
       // push this rank's partial state to the finaliser of each dim
       const uint32_t fbar = peer_addr(part_bar_l, f);
@@ -303,7 +313,7 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
         float total = 0.f;
 #pragma unroll
         for (int i = 0; i < F; ++i) total += sh.ss_recv[i];
-        finalize_slice(p, sh.fs, n, active, d0, c0, c1, mbad, meta, cs, sn, total, dbase, WD);
+        finalize_slice(p, sh.fs, layer, o, active, d0, c0, c1, mbad, meta, cs, sn, total, dbase, WD);
       } else {
         consumer_sync();  // sh.fs.red is rewritten by the next output
       }
@@ -318,7 +328,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const P
       *reinterpret_cast<ClusterShared<S>*>(smem + static_cast<size_t>(kStages) * kBlockBytes);
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
   const int64_t c = blockIdx.x / S, ncl = gridDim.x / S;
-  const int64_t N = p.num_outputs;
+  const int64_t N = p.num_outputs * p.num_layers;  // outputs of all layers
   const int64_t n0 = c * N / ncl, n1 = (c + 1) * N / ncl;
   const int K = p.blocks_per_output;
   const int k_lo = static_cast<int>(rank) * K / S;

@@ -443,7 +443,8 @@ __device__ __forceinline__ float consumer_sum_squares(FinalScratch& fs, float c0
 }
 
 // RMSNorm, NOPE quantisation, RoPE and the store of dims [dbase, dbase + wd)
-// of output n.  Thread t < wd/2 is `active` and owns dims d0 = dbase + 2t and
+// of output row `row` (= layer * num_outputs + n: the y_out row) of layer
+// `layer`.  Thread t < wd/2 is `active` and owns dims d0 = dbase + 2t and
 // d0 + 1 with window sums c0, c1; `total` is the sum of c^2 over all 512
 // dims.  wd is a multiple of 64, so every 64-dim quantisation group lies in
 // one warp and the RoPE dims 448..511 in the last.  The slice's bytes are
@@ -451,19 +452,19 @@ __device__ __forceinline__ float consumer_sum_squares(FinalScratch& fs, float c0
 // RoPE dims) and scale bytes [dbase/64, (dbase + wd)/64) (the last one is
 // the zero padding byte).  All 256 consumer threads call this (it holds
 // consumer barriers).
-__device__ __forceinline__ void finalize_slice(const Params& p, FinalScratch& fs, int64_t n,
-                                               bool active, int d0, float c0, float c1, bool bad,
-                                               const MetaRec& meta, float cs, float sn, float total,
-                                               int dbase, int wd) {
+__device__ __forceinline__ void finalize_slice(const Params& p, FinalScratch& fs, int layer,
+                                               int64_t row, bool active, int d0, float c0, float c1,
+                                               bool bad, const MetaRec& meta, float cs, float sn,
+                                               float total, int dbase, int wd) {
   const int t = threadIdx.x, lane = t & 31;
   const bool invalid = consumer_any(bad) || meta.pc < 0;
   const float rho = __frsqrt_rn(total * (1.0f / kHeadDim) + p.eps);
   if (active) {
-    const float2 w = __ldg(reinterpret_cast<const float2*>(p.weight + d0));
+    const float2 w = __ldg(reinterpret_cast<const float2*>(p.weights[layer] + d0));
     const float y0 = __fmul_rn(__fmul_rn(c0, rho), w.x);
     const float y1 = __fmul_rn(__fmul_rn(c1, rho), w.y);
     if (p.y_out != nullptr && !invalid)
-      *reinterpret_cast<float2*>(p.y_out + n * kHeadDim + d0) = make_float2(y0, y1);
+      *reinterpret_cast<float2*>(p.y_out + row * kHeadDim + d0) = make_float2(y0, y1);
     if (d0 < kNopeDim) {
       // bf16 round trip, group amax (one warp = one 64-dim group), exponent,
       // truncating codes, two's-complement bytes
@@ -491,7 +492,7 @@ __device__ __forceinline__ void finalize_slice(const Params& p, FinalScratch& fs
   }
   consumer_sync();
   if (!invalid && meta.slot >= 0) {
-    uint8_t* page = p.kv + (meta.slot / kSlotsPerPage) * kPageBytes;
+    uint8_t* page = p.kvs[layer] + (meta.slot / kSlotsPerPage) * kPageBytes;
     const int64_t off = meta.slot % kSlotsPerPage;
     const int pb0 = dbase;
     const int pb1 = (dbase + wd == kHeadDim) ? kTokenStride : dbase + wd;

@@ -38,8 +38,15 @@ constexpr int kMetaRing = kStages + 2;                     // per-output records
 // A split output's partial softmax state: m[512], den[512], num[512].
 constexpr int kPartialFloats = 3 * kHeadDim;
 
+// Layers one multi-layer call may compress (per-layer pointers travel in the
+// kernel parameters).
+constexpr int kMaxLayers = 64;
+
 struct Params {
-  const uint16_t* state;          // bf16 bits [num_blocks, 8, 1024]
+  const uint16_t* states[kMaxLayers];  // per layer: bf16 bits [num_blocks, B, 1024]
+  const float* weights[kMaxLayers];    // per layer: rms_norm_weight [512]
+  uint8_t* kvs[kMaxLayers];            // per layer: kv_cache [num_pages, 37376]
+  int num_layers;                      // L; outputs of the call = L * num_outputs
   int64_t num_blocks;
   const int32_t* token_to_req;
   const int64_t* positions;
@@ -49,14 +56,12 @@ struct Params {
   const int32_t* block_table;
   int64_t num_reqs;
   int64_t max_blocks;
-  const float* weight;
   const float* cos_sin;
   int64_t num_positions;
   const int64_t* slot_map;
   int slot_by_token;              // 1: slot_map[b], 0: slot_map[n]
-  uint8_t* kv;
   int64_t num_pages;
-  float* y_out;                   // optional
+  float* y_out;                   // optional: [L * num_outputs, 512], layer-major
   int compress_ratio;             // C
   int block_size;                 // B: rows per physical state block
   int blocks_per_output;          // K = ceil(C / 8): 8-row chunks per window

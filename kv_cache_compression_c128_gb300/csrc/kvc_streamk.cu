@@ -12,6 +12,8 @@
 // It needs no thread-block clusters; it is the route for devices or
 // configurations where the cluster route is unavailable, and it is the route
 // that uses scratch memory (the workspace, or the library's static buffer).
+// One launch compresses one layer (the layer-0 pointers of its Params); the
+// host launches it once per layer of a multi-layer call.
 //
 // Warp 8 resolves block_table entries 32 units at a time and issues one
 // cp.async.bulk of 16 KiB per unit into a kStages ring; warps 0-7 fold the
@@ -87,7 +89,7 @@ __device__ void producer(const Params& p, StreamKShared& sh, uint8_t* ring, int6
             sh.stage_ok[stage] = 1;
             mbar_arrive_expect_tx(&sh.full_bar[stage], kBlockBytes);
             bulk_copy_g2s(ring + static_cast<size_t>(stage) * kBlockBytes,
-                          p.state + gb * (kBlockRows * kRowElems), kBlockBytes,
+                          p.states[0] + gb * (kBlockRows * kRowElems), kBlockBytes,
                           &sh.full_bar[stage], policy);
           } else {
             sh.stage_ok[stage] = 0;
@@ -115,7 +117,7 @@ __device__ __forceinline__ void finalize_whole(const Params& p, StreamKShared& s
                                                float c1, bool bad, const MetaRec& meta, float cs,
                                                float sn) {
   const float total = consumer_sum_squares(sh.fs, c0, c1);
-  finalize_slice(p, sh.fs, n, true, 2 * threadIdx.x, c0, c1, bad, meta, cs, sn, total, 0, kHeadDim);
+  finalize_slice(p, sh.fs, 0, n, true, 2 * threadIdx.x, c0, c1, bad, meta, cs, sn, total, 0, kHeadDim);
 }
 
 // Store this CTA's partial state of output n; the last CTA to arrive merges

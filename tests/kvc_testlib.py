@@ -115,3 +115,65 @@ def run_gpu(case, flags=0, dev_arrays=None, slot_mapping=None):
                               rms_norm_eps=case.rms_norm_eps, y_out=y, flags=flags, **d)
     err = kvc.kvc_get_device_error(torch.cuda.current_stream().cuda_stream)
     return d["kv_cache"].cpu().numpy(), y[:N].cpu().numpy(), err
+
+
+# ---- the parity bar (see tests/test_gpu_parity.py for its statement) -----------
+
+Y_RTOL = 2e-3
+Y_ATOL_RMS = 1e-5
+
+
+def _y_ok(y_gpu, y_ref):
+    rms = np.sqrt((y_ref.astype(np.float64) ** 2).mean(1, keepdims=True))
+    err = np.abs(y_gpu.astype(np.float64) - y_ref)
+    return np.all(err <= Y_RTOL * np.abs(y_ref) + Y_ATOL_RMS * rms), float(
+        (err / (np.abs(y_ref) + rms)).max())
+
+
+def assert_parity(oracle_mod, case, kv_g, y_g):
+    """The three-way parity bar between GPU results (kv bytes, y) and the
+    oracle on `case`: y within 2e-3 relative; kv bytes bit-exact against the
+    oracle's finalizer applied to the GPU's y; against the oracle's own bytes
+    within one quantisation step / one scale step / a bf16 ulp plus the y
+    tolerance, every other byte untouched.  Returns stats."""
+    kv_o, res = oracle_mod.compress_case(case)
+    assert res["status"] == 0
+    ok, worst = _y_ok(y_g, res["y"])
+    assert ok, f"y outside 2e-3 relative (worst scaled error {worst:.3g})"
+
+    # (2) bytes exactly determined by the GPU's y
+    kv_y = case.kv_cache.copy()
+    oracle_mod.quant_rope_scatter(y_g, case.positions, case.boundary_token_indices,
+                                  case.compress_ratio, case.cos_sin_cache,
+                                  case.kv_slot_mapping, kv_y)
+    if not np.array_equal(kv_g, kv_y):
+        bad = np.nonzero(kv_g.reshape(-1) != kv_y.reshape(-1))[0]
+        raise AssertionError(f"{bad.size} bytes differ from oracle(y_gpu); first at {bad[:8]}")
+
+    # (3) against the oracle's own bytes
+    slots = slots_of_case(case)
+    m = written_mask(kv_g.shape, slots)
+    assert np.array_equal(kv_g.reshape(-1)[~m], kv_o.reshape(-1)[~m])
+    assert np.array_equal(kv_g.reshape(-1)[~m], case.kv_cache.reshape(-1)[~m])
+    n_code_diff = 0
+    y_rms = np.sqrt((res["y"].astype(np.float64) ** 2).mean(1))
+    for n, s in enumerate(slots):
+        if s < 0:
+            continue
+        qg, eg, pg, rg = decode_slot(kv_g, s)
+        qo, eo, po, ro = decode_slot(kv_o, s)
+        assert pg == 0 and po == 0
+        assert np.all(np.abs(eg - eo) <= 1)
+        step = np.maximum(np.repeat(np.ldexp(1.0, eg), 64), np.repeat(np.ldexp(1.0, eo), 64))
+        assert np.all(np.abs(dequant(qg, eg) - dequant(qo, eo)) <= step)
+        mag = np.maximum(np.abs(ro), np.abs(rg))
+        ulp = np.ldexp(1.0, np.frexp(np.maximum(mag, 1e-30))[1] - 8)
+        pair = np.repeat(np.hypot(res["y"][n, 448::2], res["y"][n, 449::2]), 2)
+        tol = ulp + Y_RTOL * pair + 1.5 * Y_ATOL_RMS * y_rms[n]
+        assert np.all(np.abs(rg.astype(np.float64) - ro) <= tol)
+        n_code_diff += int(np.sum(qg != qo))
+    # differing codes come only from y values within rounding of a code edge
+    assert n_code_diff <= max(8, 2e-3 * 448 * max(1, case.num_outputs))
+    return {"worst_y": worst, "code_diff": n_code_diff}
+
+

@@ -146,3 +146,18 @@ def test_dequantize_host_validation(kvc, change, status):
 
 def test_dequantize_zero_slots_is_a_no_op(kvc):
     assert kvc.kvc_dequantize(0x10000, 1, 0x20000, 0, 0x30000, 0, 0) == 0
+
+
+def test_layers_host_validation(kvc):
+    args = dict(_GOOD)
+    for k in ("state_cache", "rms_norm_weight", "kv_cache"):
+        args.pop(k)
+    base = dict(num_layers=2, state_caches=[0x10000, 0x11000], rms_norm_weights=[0x60000, 0x61000],
+                kv_caches=[0x90000, 0x91000], **args)
+    assert kvc.kvc_compress_layers(**dict(base, num_layers=0)) == 1
+    assert kvc.kvc_compress_layers(**dict(base, num_layers=65, state_caches=[0x10000] * 65,
+                                          rms_norm_weights=[0x60000] * 65,
+                                          kv_caches=[0x90000] * 65)) == 1
+    assert kvc.kvc_compress_layers(**dict(base, state_caches=[0x10000, 0])) == 1
+    assert kvc.kvc_compress_layers(**dict(base, kv_caches=[0x90000, 0x91004])) == 1
+    assert kvc.kvc_compress_layers(**dict(base, num_outputs=0)) == 0
