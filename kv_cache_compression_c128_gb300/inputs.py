@@ -34,6 +34,18 @@ Recipe (every array is a pure function of the shape and the seed):
   permutation of ``0..N-1`` at the boundary tokens.
 * ``kv_cache``: uint8 ``[ceil(N/64), 64*576 + 64*8]`` filled with zeros (or a
   seeded byte pattern, for the untouched-bytes tests).
+
+Layout variants (the fp32 state the page's traffic count of "The Baseline"
+assumes, and the explicit block / row / column strides of "A Bit of Triton
+and GPU Background"):
+
+* ``fp32_state``: fp32 ``[T/8, 8, 1024]``, N(0,1) drawn from its own seed and
+  kept in fp32 (most values are not representable in bf16).
+* ``embed_strided``: places a state in a larger flat buffer at element
+  ``g * block_stride + o * row_stride + col``; every other element holds a
+  poison value (NaN by default), so a stride mistake cannot go unnoticed.
+* ``strided_table``: the same for the block table, entry ``(r, l)`` at
+  ``r * row_stride + l * col_stride``, the rest -1.
 """
 from __future__ import annotations
 
@@ -196,6 +208,41 @@ def make_case(num_reqs: int, total_tokens: int, compress_ratio: int, *,
                 positions=positions, boundary_token_indices=bti,
                 block_table=block_table, rms_norm_weight=weight,
                 cos_sin_cache=csc, kv_slot_mapping=slot_map, kv_cache=kv)
+
+
+def fp32_state(num_blocks: int, block_size: int, seed: int) -> np.ndarray:
+    """fp32 state [num_blocks, block_size, 1024] drawn N(0,1), seed `seed`."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.standard_normal((num_blocks, block_size, STATE_WIDTH), dtype=np.float32)
+
+
+def embed_strided(state: np.ndarray, block_stride: int, row_stride: int,
+                  fill=None) -> np.ndarray:
+    """Flat copy of `state` ([G, B, 1024], uint16 bf16 bits or float32) with
+    element (g, o, col) at g * block_stride + o * row_stride + col; every
+    other element holds `fill` (default: a quiet NaN of the dtype)."""
+    G, B, W = state.shape
+    assert W == STATE_WIDTH and row_stride >= W and block_stride >= (B - 1) * row_stride + W
+    size = (G - 1) * block_stride + (B - 1) * row_stride + W
+    if fill is None:
+        fill = np.uint16(0x7FC1) if state.dtype == np.uint16 else np.float32(np.nan)
+    out = np.full(size, fill, dtype=state.dtype)
+    idx = (np.arange(G)[:, None, None] * block_stride + np.arange(B)[None, :, None] * row_stride
+           + np.arange(W)[None, None, :])
+    out[idx] = state
+    return out
+
+
+def strided_table(block_table: np.ndarray, row_stride: int, col_stride: int) -> np.ndarray:
+    """Flat int32 copy of `block_table` ([R, M]) with entry (r, l) at
+    r * row_stride + l * col_stride; other entries hold -1."""
+    R, M = block_table.shape
+    size = (R - 1) * row_stride + (M - 1) * col_stride + 1
+    out = np.full(size, -1, dtype=np.int32)
+    idx = np.arange(R)[:, None] * row_stride + np.arange(M)[None, :] * col_stride
+    assert np.unique(idx).size == idx.size
+    out[idx] = block_table
+    return out
 
 
 def ragged_lengths(num_reqs: int, total_tokens: int, compress_ratio: int,

@@ -65,6 +65,9 @@ def _load():
             lib.kvc_oracle_window_reduce.argtypes = [
                 P, I64, I32, P, P, I64, P, I64, P, I64, I64, I32, P, P]
             lib.kvc_oracle_window_reduce.restype = ctypes.c_int
+            lib.kvc_oracle_window_reduce_ex.argtypes = [
+                P, I32, I64, I64, I64, I32, P, P, I64, P, I64, P, I64, I64, I64, I64, I32, P, P]
+            lib.kvc_oracle_window_reduce_ex.restype = ctypes.c_int
             lib.kvc_oracle_rmsnorm.argtypes = [P, P, F32, I64, P]
             lib.kvc_oracle_rmsnorm.restype = None
             lib.kvc_oracle_pack_slot.argtypes = [P, P, P, P]
@@ -76,6 +79,10 @@ def _load():
                 P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P,
                 I64, I32, I32, F32, P, P, P]
             lib.kvc_oracle_compress.restype = ctypes.c_int
+            lib.kvc_oracle_compress_ex.argtypes = [
+                P, I32, I64, I64, I64, P, P, I64, P, I64, P, I64, I64, I64, I64, P, P, I64, P,
+                I64, P, I64, I32, I32, F32, P, P, P]
+            lib.kvc_oracle_compress_ex.restype = ctypes.c_int
             lib.kvc_oracle_dequantize.argtypes = [P, I64, P, I64, P, I32]
             lib.kvc_oracle_dequantize.restype = ctypes.c_int
             _lib = lib
@@ -135,6 +142,31 @@ def window_reduce(state_bits, token_to_req, positions, boundary_token_indices,
         _ptr(st), st.shape[0], block_size, _ptr(t2r), _ptr(pos), pos.shape[0],
         _ptr(bti), N, _ptr(bt), bt.shape[0], bt.shape[1], compress_ratio,
         _ptr(c), _ptr(valid))
+    return c, valid, int(status)
+
+
+def window_reduce_ex(state, block_stride, row_stride, num_blocks, block_size, token_to_req,
+                     positions, boundary_token_indices, block_table, max_blocks_per_req,
+                     bt_row_stride, bt_col_stride, compress_ratio):
+    """window_reduce over a strided state: `state` is a flat numpy array of
+    uint16 (bf16 bits) or float32 elements, addressed as block g, row o,
+    column col at g * block_stride + o * row_stride + col; block_table is a
+    flat int32 array addressed as r * bt_row_stride + l * bt_col_stride."""
+    st = np.ascontiguousarray(state).reshape(-1)
+    dtype = 2 if st.dtype == np.float32 else 1
+    assert st.dtype in (np.float32, np.uint16)
+    t2r = _c(token_to_req, np.int32)
+    pos = _c(positions, np.int64)
+    bti = _c(boundary_token_indices, np.int64)
+    bt = _c(block_table, np.int32).reshape(-1)
+    N = bti.shape[0]
+    num_reqs = int(t2r.max()) + 1 if t2r.size else 1
+    c = np.zeros((N, HEAD_DIM), dtype=np.float32)
+    valid = np.zeros(N, dtype=np.uint8)
+    status = _load().kvc_oracle_window_reduce_ex(
+        _ptr(st), dtype, block_stride, row_stride, num_blocks, block_size, _ptr(t2r), _ptr(pos),
+        pos.shape[0], _ptr(bti), N, _ptr(bt), num_reqs, max_blocks_per_req, bt_row_stride,
+        bt_col_stride, compress_ratio, _ptr(c), _ptr(valid))
     return c, valid, int(status)
 
 
@@ -199,6 +231,39 @@ def compress(state_bits, token_to_req, positions, boundary_token_indices,
         _ptr(bt), bt.shape[0], bt.shape[1], _ptr(w), _ptr(csc), csc.shape[0],
         _ptr(sm), sm.shape[0], _ptr(kv_cache), kv_cache.shape[0], block_size,
         compress_ratio, float(rms_norm_eps), _ptr(c), _ptr(y), _ptr(valid))
+    return {"c": c, "y": y, "valid": valid, "status": int(status)}
+
+
+def compress_strided(state, block_stride, row_stride, num_blocks, token_to_req, positions,
+                     boundary_token_indices, block_table, num_reqs, max_blocks_per_req,
+                     bt_row_stride, bt_col_stride, rms_norm_weight, cos_sin_cache,
+                     kv_slot_mapping, kv_cache, block_size, compress_ratio, rms_norm_eps=1e-6):
+    """compress over a strided state of bf16 bits (uint16) or float32: `state`
+    is a flat array addressed as g * block_stride + o * row_stride + col, and
+    `block_table` a flat int32 array addressed as r * bt_row_stride +
+    l * bt_col_stride.  kv_cache (uint8) is written in place; returns the same
+    dict as compress."""
+    st = np.ascontiguousarray(state).reshape(-1)
+    assert st.dtype in (np.float32, np.uint16)
+    dtype = 2 if st.dtype == np.float32 else 1
+    t2r = _c(token_to_req, np.int32)
+    pos = _c(positions, np.int64)
+    bti = _c(boundary_token_indices, np.int64)
+    bt = _c(block_table, np.int32).reshape(-1)
+    w = _c(rms_norm_weight, np.float32)
+    csc = _c(cos_sin_cache, np.float32)
+    sm = _c(kv_slot_mapping, np.int64)
+    assert kv_cache.flags.c_contiguous and kv_cache.dtype == np.uint8
+    N = bti.shape[0]
+    c = np.zeros((N, HEAD_DIM), dtype=np.float32)
+    y = np.zeros((N, HEAD_DIM), dtype=np.float32)
+    valid = np.zeros(N, dtype=np.uint8)
+    status = _load().kvc_oracle_compress_ex(
+        _ptr(st), dtype, block_stride, row_stride, num_blocks, _ptr(t2r), _ptr(pos),
+        pos.shape[0], _ptr(bti), N, _ptr(bt), num_reqs, max_blocks_per_req, bt_row_stride,
+        bt_col_stride, _ptr(w), _ptr(csc), csc.shape[0], _ptr(sm), sm.shape[0],
+        _ptr(kv_cache), kv_cache.shape[0], block_size, compress_ratio, float(rms_norm_eps),
+        _ptr(c), _ptr(y), _ptr(valid))
     return {"c": c, "y": y, "valid": valid, "status": int(status)}
 
 

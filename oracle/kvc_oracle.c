@@ -12,7 +12,10 @@
  *   "How One Output Is Produced"   - window, paged addressing, per-dimension
  *                                    softmax sum, RMSNorm, NOPE quantisation,
  *                                    GPT-J RoPE and the scatter address,
- *   "The Baseline"                 - gather-then-softmax semantics,
+ *   "The Baseline"                 - gather-then-softmax semantics, and its
+ *                                    traffic count with an fp32 state element,
+ *   "A Bit of Triton and GPU Background" - the state read through explicit
+ *                                    block / row / column strides,
  *   "The Finalizer's Sharp Edges"  - fp32 finalizer, bf16 round trip,
  *                                    truncation toward zero, byte encoding.
  *
@@ -21,6 +24,9 @@
  * the tighter route and rounds c to float at the end).  The finalizer (y,
  * quantisation, RoPE) is evaluated in fp32 exactly as the page's finalizer
  * does, one rounded operation at a time; build with -ffp-contract=off.
+ *
+ * The state may be bf16 or fp32 and strided (kvc_oracle_*_ex): every element
+ * is widened exactly to double, so both dtypes follow one definition.
  *
  * The reader direction (kvc_oracle_dequantize) decodes a packed slot back to
  * a 512-vector: NOPE values q * 2^(scale - 127), RoPE values as stored.
@@ -103,25 +109,38 @@ int kvc_oracle_scale_exponent(float a) {
 
 /* ---- step 1+2: window gather and per-dimension softmax sum ----------- */
 
+/* Element `col` of physical row (g, o) of the state, widened exactly to
+ * double.  state_dtype 1 = bf16, 2 = fp32; strides in elements. */
+static double or_state_elem(const void* state, int state_dtype, int64_t block_stride,
+                            int64_t row_stride, int64_t g, int64_t o, int64_t col) {
+  int64_t idx = g * block_stride + o * row_stride + col;
+  if (state_dtype == 2) return (double)((const float*)state)[idx];
+  return (double)or_bf16_bits_to_float(((const uint16_t*)state)[idx]);
+}
+
 /*
  * For each output n (boundary token b = boundary_token_indices[n]):
  *   r = token_to_req[b], p = positions[b], t_i = p - C + 1 + i (0 <= i < C),
  *   l_i = floor(t_i / B), o_i = t_i mod B, g_i = block_table[r, l_i],
- *   row_i = g_i * B + o_i; v = state[row_i, 0:512], s = state[row_i, 512:1024]
+ *   row_i = (g_i, o_i); v = state[row_i, 0:512], s = state[row_i, 512:1024]
  *   c_d = sum_i softmax_i(s_{., d}) * v_{i, d}   (softmax along the window).
  * Two-pass softmax in double: max, then sum of exp and weighted sum.
+ * The state is bf16 (state_dtype 1) or fp32 (2) with the given element
+ * strides between physical blocks and between rows of a block (columns are
+ * contiguous); block_table[r, l] is at r * bt_row_stride + l * bt_col_stride.
  * c is written as float [N, 512].  Returns OR_BAD_INDEX on any index that
  * falls outside its array; nothing is written for that output then and
  * valid_out[n] (if valid_out is not NULL) is set to 0, else to 1.
  */
-int kvc_oracle_window_reduce(
-    const uint16_t* state, int64_t num_state_blocks, int32_t block_size,
+int kvc_oracle_window_reduce_ex(
+    const void* state, int32_t state_dtype, int64_t state_block_stride,
+    int64_t state_row_stride, int64_t num_state_blocks, int32_t block_size,
     const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
     const int64_t* boundary_token_indices, int64_t num_outputs,
     const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    int64_t bt_row_stride, int64_t bt_col_stride,
     int32_t compress_ratio, float* c_out, uint8_t* valid_out) {
   const int64_t C = compress_ratio, B = block_size;
-  const int64_t W = 2 * OR_HEAD_DIM;
   int status = OR_OK;
   double m[OR_HEAD_DIM], den[OR_HEAD_DIM], num[OR_HEAD_DIM];
   for (int64_t n = 0; n < num_outputs; ++n) {
@@ -137,7 +156,7 @@ int kvc_oracle_window_reduce(
       int64_t t = p - C + 1 + i;
       int64_t l = t / B;
       if (l >= max_blocks_per_req) { ok = 0; break; }
-      int64_t g = block_table[r * max_blocks_per_req + l];
+      int64_t g = block_table[r * bt_row_stride + l * bt_col_stride];
       if (g < 0 || g >= num_state_blocks) ok = 0;
     }
     if (!ok) { status = OR_BAD_INDEX; continue; }
@@ -145,23 +164,25 @@ int kvc_oracle_window_reduce(
     /* pass 1: per-dimension maximum of the scores */
     for (int64_t i = 0; i < C; ++i) {
       int64_t t = p - C + 1 + i;
-      int64_t row = (int64_t)block_table[r * max_blocks_per_req + t / B] * B + t % B;
-      const uint16_t* s = state + row * W + OR_HEAD_DIM;
+      int64_t g = block_table[r * bt_row_stride + (t / B) * bt_col_stride];
       for (int d = 0; d < OR_HEAD_DIM; ++d) {
-        double sd = (double)or_bf16_bits_to_float(s[d]);
+        double sd = or_state_elem(state, state_dtype, state_block_stride, state_row_stride, g,
+                                  t % B, OR_HEAD_DIM + d);
         if (sd > m[d]) m[d] = sd;
       }
     }
     /* pass 2: denominators and weighted numerators */
     for (int64_t i = 0; i < C; ++i) {
       int64_t t = p - C + 1 + i;
-      int64_t row = (int64_t)block_table[r * max_blocks_per_req + t / B] * B + t % B;
-      const uint16_t* v = state + row * W;
-      const uint16_t* s = v + OR_HEAD_DIM;
+      int64_t g = block_table[r * bt_row_stride + (t / B) * bt_col_stride];
       for (int d = 0; d < OR_HEAD_DIM; ++d) {
-        double e = exp((double)or_bf16_bits_to_float(s[d]) - m[d]);
+        double sd = or_state_elem(state, state_dtype, state_block_stride, state_row_stride, g,
+                                  t % B, OR_HEAD_DIM + d);
+        double vd = or_state_elem(state, state_dtype, state_block_stride, state_row_stride, g,
+                                  t % B, d);
+        double e = exp(sd - m[d]);
         den[d] += e;
-        num[d] += e * (double)or_bf16_bits_to_float(v[d]);
+        num[d] += e * vd;
       }
     }
     for (int d = 0; d < OR_HEAD_DIM; ++d)
@@ -169,6 +190,21 @@ int kvc_oracle_window_reduce(
     if (valid_out) valid_out[n] = 1;
   }
   return status;
+}
+
+/* The same for a contiguous bf16 state [num_blocks, B, 1024] and a
+ * row-major block_table [num_reqs, max_blocks_per_req]. */
+int kvc_oracle_window_reduce(
+    const uint16_t* state, int64_t num_state_blocks, int32_t block_size,
+    const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
+    const int64_t* boundary_token_indices, int64_t num_outputs,
+    const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    int32_t compress_ratio, float* c_out, uint8_t* valid_out) {
+  const int64_t W = 2 * OR_HEAD_DIM;
+  return kvc_oracle_window_reduce_ex(
+      state, 1, (int64_t)block_size * W, W, num_state_blocks, block_size, token_to_req,
+      positions, num_tokens, boundary_token_indices, num_outputs, block_table, num_reqs,
+      max_blocks_per_req, max_blocks_per_req, 1, compress_ratio, c_out, valid_out);
 }
 
 /* ---- step 3: RMSNorm ------------------------------------------------ */
@@ -291,6 +327,33 @@ int kvc_oracle_quant_rope_scatter(
  * whose window has an index outside its array is skipped; the other
  * outputs are still written and OR_BAD_INDEX is returned.
  */
+int kvc_oracle_compress_ex(
+    const void* state, int32_t state_dtype, int64_t state_block_stride,
+    int64_t state_row_stride, int64_t num_state_blocks,
+    const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
+    const int64_t* boundary_token_indices, int64_t num_outputs,
+    const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    int64_t bt_row_stride, int64_t bt_col_stride,
+    const float* rms_norm_weight, const float* cos_sin_cache,
+    int64_t num_positions, const int64_t* kv_slot_mapping,
+    int64_t slot_mapping_len, uint8_t* kv_cache, int64_t num_kv_pages,
+    int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
+    float* c, float* y, uint8_t* valid) {
+  memset(c, 0, sizeof(float) * (size_t)(num_outputs * OR_HEAD_DIM));
+  int st1 = kvc_oracle_window_reduce_ex(
+      state, state_dtype, state_block_stride, state_row_stride, num_state_blocks, block_size,
+      token_to_req, positions, num_tokens, boundary_token_indices, num_outputs, block_table,
+      num_reqs, max_blocks_per_req, bt_row_stride, bt_col_stride, compress_ratio, c, valid);
+  kvc_oracle_rmsnorm(c, rms_norm_weight, rms_norm_eps, num_outputs, y);
+  int st2 = kvc_oracle_quant_rope_scatter(
+      y, valid, num_outputs, boundary_token_indices, positions, num_tokens,
+      compress_ratio, cos_sin_cache, num_positions, kv_slot_mapping,
+      slot_mapping_len, kv_cache, num_kv_pages);
+  return st1 != OR_OK ? st1 : st2;
+}
+
+/* kvc_oracle_compress_ex for a contiguous bf16 state [num_blocks, B, 1024]
+ * and a row-major block_table [num_reqs, max_blocks_per_req]. */
 int kvc_oracle_compress(
     const uint16_t* state, int64_t num_state_blocks,
     const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
@@ -301,17 +364,13 @@ int kvc_oracle_compress(
     int64_t slot_mapping_len, uint8_t* kv_cache, int64_t num_kv_pages,
     int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
     float* c, float* y, uint8_t* valid) {
-  memset(c, 0, sizeof(float) * (size_t)(num_outputs * OR_HEAD_DIM));
-  int st1 = kvc_oracle_window_reduce(
-      state, num_state_blocks, block_size, token_to_req, positions, num_tokens,
-      boundary_token_indices, num_outputs, block_table, num_reqs,
-      max_blocks_per_req, compress_ratio, c, valid);
-  kvc_oracle_rmsnorm(c, rms_norm_weight, rms_norm_eps, num_outputs, y);
-  int st2 = kvc_oracle_quant_rope_scatter(
-      y, valid, num_outputs, boundary_token_indices, positions, num_tokens,
-      compress_ratio, cos_sin_cache, num_positions, kv_slot_mapping,
-      slot_mapping_len, kv_cache, num_kv_pages);
-  return st1 != OR_OK ? st1 : st2;
+  const int64_t W = 2 * OR_HEAD_DIM;
+  return kvc_oracle_compress_ex(
+      state, 1, (int64_t)block_size * W, W, num_state_blocks, token_to_req, positions,
+      num_tokens, boundary_token_indices, num_outputs, block_table, num_reqs,
+      max_blocks_per_req, max_blocks_per_req, 1, rms_norm_weight, cos_sin_cache,
+      num_positions, kv_slot_mapping, slot_mapping_len, kv_cache, num_kv_pages, block_size,
+      compress_ratio, rms_norm_eps, c, y, valid);
 }
 
 /*
