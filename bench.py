@@ -186,10 +186,12 @@ class ClockSampler:
 def _tensors(case, device, copies):
     import torch
 
-    st_host = torch.from_numpy(case.state_bits.view(np.int16)).view(torch.bfloat16)
-    states = [st_host.to(device)]
-    for _ in range(copies - 1):
-        states.append(states[0].clone())
+    states = []
+    if copies > 0:
+        st_host = torch.from_numpy(case.state_bits.view(np.int16)).view(torch.bfloat16)
+        states = [st_host.to(device)]
+        for _ in range(copies - 1):
+            states.append(states[0].clone())
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
     d = dict(token_to_req=t(case.token_to_req), positions=t(case.positions),
              boundary_token_indices=t(case.boundary_token_indices),
@@ -205,12 +207,20 @@ def _copies_for(case) -> int:
 
 
 def time_device(kvc, case, device, steps: int, warmup: int, sampler=None,
-                graph_chunk: int = 250):
-    """Average seconds per call over `steps` graph-replayed launches."""
+                graph_chunk: int = 250, states=None, block_table=None):
+    """Average seconds per call over `steps` graph-replayed launches.
+    `states` (rotating state tensors, any layout) and `block_table` replace
+    the case's own contiguous bf16 state and table when given."""
     import torch
 
-    copies = _copies_for(case)
-    states, d = _tensors(case, device, copies)
+    if states is None:
+        copies = _copies_for(case)
+        states, d = _tensors(case, device, copies)
+    else:
+        copies = len(states)
+        _, d = _tensors(case, device, 0)
+    if block_table is not None:
+        d = dict(d, block_table=block_table)
     stream = torch.cuda.Stream(device)
     N = case.num_outputs
     ws = torch.zeros(kvc.kvc_workspace_bytes(N), dtype=torch.uint8, device=device)
@@ -409,13 +419,59 @@ def time_oracle(case, max_outputs: int):
     return dt, n
 
 
-def bytes_for(case, n_outputs=None) -> int:
-    """Algorithmic bytes of a call: state rows, block-table entries (one per
-    8-row chunk of the window, two where a chunk straddles blocks; counted
-    as one), per-output metadata, one cos/sin row, the weights, the slot."""
+def bytes_for(case, n_outputs=None, elem_bytes: int = 2) -> int:
+    """Algorithmic bytes of a call: state rows (1024 elements of elem_bytes),
+    block-table entries (one per 8-row chunk of the window, two where a
+    chunk straddles blocks; counted as one), per-output metadata, one
+    cos/sin row, the weights, the slot."""
     n = case.num_outputs if n_outputs is None else n_outputs
     c = case.compress_ratio
-    return n * c * 2048 + n * (-(-c // 8)) * 4 + n * 28 + n * 256 + 2048 + n * 584
+    return (n * c * 1024 * elem_bytes + n * (-(-c // 8)) * 4 + n * 28 + n * 256 + 2048
+            + n * 584)
+
+
+def time_layouts(kvc, device, peak: float, steps: int = 600):
+    """The headline shape with the state in other layouts: fp32 elements
+    (contiguous), bf16 rows 64 elements apart (one bulk copy per row), and
+    bf16 blocks 512 elements apart with a column-major block table.  Each
+    layout is built on the device from the case's seeded values, three
+    rotating copies (> L2)."""
+    import torch
+
+    from kv_cache_compression_c128_gb300 import inputs
+
+    case = inputs.headline_case()
+    G, B = case.num_state_blocks, case.block_size
+    R, M = case.block_table.shape
+    bits = torch.from_numpy(case.state_bits.view(np.int16)).view(torch.bfloat16).to(device)
+    table_cm = torch.from_numpy(inputs.strided_table(case.block_table, 1, R)).to(device)
+    table_cm = table_cm.as_strided((R, M), (1, R))
+
+    def embedded(src, rs, bs):
+        size = (G - 1) * bs + (B - 1) * rs + 1024
+        flat = torch.full((size,), float("nan"), dtype=src.dtype, device=device)
+        view = flat.as_strided((G, B, 1024), (bs, rs, 1))
+        view.copy_(src)
+        return view
+
+    variants = [
+        ("fp32_contiguous", 4, lambda: bits.float(), None),
+        ("bf16_rows_64_apart", 2, lambda: embedded(bits, 1088, 8 * 1088), None),
+        ("bf16_blocks_512_apart_colmajor_table", 2, lambda: embedded(bits, 1024, 8 * 1024 + 512),
+         table_cm),
+    ]
+    out = []
+    for name, eb, make, table in variants:
+        states = [make() for _ in range(3)]
+        t, _ = time_device(kvc, case, device, steps, 20, states=states, block_table=table)
+        b = bytes_for(case, elem_bytes=eb)
+        dt = kvc.KVC_DTYPE_F32 if eb == 4 else kvc.KVC_DTYPE_BF16
+        ctas, clu, _, _ = kvc.kvc_query_launch_ex(case.num_outputs, case.compress_ratio, dt)
+        out.append({"layout": name, "shape": case.name, "bytes": b, "ctas": ctas,
+                    "cluster_size": clu, "us_per_call": round(t * 1e6, 3),
+                    "gb_s": round(b / t / 1e9, 1), "pct_of_peak": round(100 * b / t / 1e9 / peak, 1)})
+        del states
+    return out
 
 
 # ---- main ------------------------------------------------------------------------
@@ -482,6 +538,7 @@ def main():
 
     reader = time_reader(kvc, case, device) if rank == 0 else None
     layers = time_layers(kvc, inputs.bench_case(0), device, 8) if rank == 0 else None
+    layouts = time_layouts(kvc, device, peak) if rank == 0 and not args.no_sweep else None
 
     sweep = None
     if not args.no_sweep and rank == 0:
@@ -544,6 +601,7 @@ def main():
         "e2e": e2e,
         "reader": reader,
         "layers": layers,
+        "layouts": layouts,
         "cpu_baseline": cpu,
         "sweep": sweep,
         "kernel_source_hash": kernel_source_hash(),

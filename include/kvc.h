@@ -40,9 +40,11 @@ typedef enum {
   KVC_OK = 0,
   KVC_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, small workspace */
   KVC_ERR_UNSUPPORTED = 2,  /* block_size < 8; a cluster size the problem or device
-                               cannot take; the stream-K route asked for with
-                               block_size != 8 or C not a multiple of 8, or (device,
-                               stream-K route) a window not starting on an 8-row block */
+                               cannot take; a state stride that is not a multiple of
+                               16 bytes; the stream-K route asked for with block_size
+                               != 8, C not a multiple of 8, an fp32 state or rows of
+                               a block that are not adjacent, or (device, stream-K
+                               route) a window not starting on an 8-row block */
   KVC_ERR_CUDA = 3,         /* a CUDA runtime call failed */
   KVC_ERR_BAD_INDEX = 4,    /* (device) an index outside its array */
   KVC_ERR_TIMEOUT = 5,      /* (device) a pipeline wait ran past its limit */
@@ -64,6 +66,11 @@ typedef enum {
 #define KVC_FLAG_CLUSTER_MASK (0x1Fu << KVC_FLAG_CLUSTER_SHIFT)
 #define KVC_FLAG_STREAM_K (1u << 24)
 #define KVC_FLAG_ALL (KVC_FLAG_GRID_MASK | KVC_FLAG_CLUSTER_MASK | KVC_FLAG_STREAM_K)
+
+/* Element types: of the state (kvc_compress_strided, kvc_query_launch_ex)
+ * and of the output of kvc_dequantize. */
+#define KVC_DTYPE_F32 0
+#define KVC_DTYPE_BF16 1
 
 /*
  * Bytes of device workspace kvc_compress needs for num_outputs outputs on
@@ -154,9 +161,50 @@ kvc_status kvc_compress_layers(
     float* y_out, void* workspace, size_t workspace_bytes,
     uint32_t flags, void* stream);
 
-/* Output element types of kvc_dequantize. */
-#define KVC_DTYPE_F32 0
-#define KVC_DTYPE_BF16 1
+/*
+ * kvc_compress over a state of either element type, laid out with explicit
+ * strides, and a strided block table.  "The Baseline" of the write-up counts
+ * the window's source traffic with an fp32 state element, and "A Bit of
+ * Triton and GPU Background" reads the state through block / row / column
+ * strides; this entry point takes both.  (kvc_compress is this call with a
+ * contiguous bf16 state and a row-major block table.)
+ *
+ * state_cache         bf16 (state_dtype KVC_DTYPE_BF16) or fp32
+ *                     (KVC_DTYPE_F32) elements, 16-byte aligned.  Element
+ *                     (g, o, col) of physical block g < num_state_blocks,
+ *                     row o < block_size, column col < 1024 is at element
+ *                     offset g * state_block_stride + o * state_row_stride +
+ *                     col (columns are contiguous); the caller guarantees
+ *                     that every such element lies in the buffer.
+ * state_block_stride, state_row_stride
+ *                     >= 0, in elements; each a multiple of 16 bytes
+ *                     (KVC_ERR_UNSUPPORTED otherwise: the rows are moved by
+ *                     bulk copies).  Rows that are adjacent (row stride 1024)
+ *                     are copied a run at a time, others one row at a time.
+ * block_table         int32; entry (r, l) of request r < num_reqs, logical
+ *                     block l < max_blocks_per_req at element offset
+ *                     r * block_table_row_stride + l * block_table_col_stride
+ *                     (both >= 0; e.g. 1 and num_reqs for a column-major
+ *                     table), 4-byte aligned.
+ * Everything else (arguments, results, errors, flags) as for kvc_compress.
+ * The results are those of kvc_compress on the same values: the window sum
+ * runs in fp32 over the elements as stored (bf16 widened exactly).  The
+ * stream-K route takes only a bf16 state with adjacent rows.
+ */
+kvc_status kvc_compress_strided(
+    const void* state_cache, int32_t state_dtype, int64_t num_state_blocks,
+    int64_t state_block_stride, int64_t state_row_stride,
+    const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
+    const int64_t* boundary_token_indices, int64_t num_outputs,
+    const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    int64_t block_table_row_stride, int64_t block_table_col_stride,
+    const float* rms_norm_weight,
+    const float* cos_sin_cache, int64_t num_positions,
+    const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+    uint8_t* kv_cache, int64_t num_kv_pages,
+    int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
+    float* y_out, void* workspace, size_t workspace_bytes,
+    uint32_t flags, void* stream);
 
 /*
  * Read packed slots back as 512-vectors (the reader side of the cache: the
@@ -228,6 +276,16 @@ kvc_status kvc_compress_static(
 kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio,
                             uint32_t flags, int32_t* ctas, int32_t* cluster_size,
                             int32_t* threads, int32_t* smem_bytes);
+
+/*
+ * kvc_query_launch for a state of element type state_dtype (KVC_DTYPE_BF16
+ * or KVC_DTYPE_F32): the launch kvc_compress_strided would use.
+ * kvc_query_launch is this call with KVC_DTYPE_BF16.
+ */
+kvc_status kvc_query_launch_ex(int64_t num_outputs, int32_t compress_ratio,
+                               int32_t state_dtype, uint32_t flags, int32_t* ctas,
+                               int32_t* cluster_size, int32_t* threads,
+                               int32_t* smem_bytes);
 
 /*
  * Synchronises `stream`, then reads and clears the device error code

@@ -142,8 +142,14 @@ def lib():
             L.kvc_compress_layers.restype = ctypes.c_int
             L.kvc_dequantize.argtypes = [P, I64, P, I64, P, I32, P]
             L.kvc_dequantize.restype = ctypes.c_int
+            L.kvc_compress_strided.argtypes = [
+                P, I32, I64, I64, I64, P, P, I64, P, I64, P, I64, I64, I64, I64, P, P, I64, P,
+                I64, P, I64, I32, I32, ctypes.c_float, P, P, ctypes.c_size_t, U32, P]
+            L.kvc_compress_strided.restype = ctypes.c_int
             L.kvc_query_launch.argtypes = [I64, I32, U32, P, P, P, P]
             L.kvc_query_launch.restype = ctypes.c_int
+            L.kvc_query_launch_ex.argtypes = [I64, I32, I32, U32, P, P, P, P]
+            L.kvc_query_launch_ex.restype = ctypes.c_int
             L.kvc_get_device_error.argtypes = [P, P]
             L.kvc_get_device_error.restype = ctypes.c_int
             L.kvc_error_string.argtypes = [ctypes.c_int]
@@ -179,6 +185,18 @@ def kvc_query_launch(num_outputs: int, compress_ratio: int, flags: int = 0):
     return c.value, k.value, t.value, s.value
 
 
+def kvc_query_launch_ex(num_outputs: int, compress_ratio: int, state_dtype: int,
+                        flags: int = 0):
+    """kvc_query_launch for a state of element type state_dtype (KVC_DTYPE_*)."""
+    c, k, t, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    st = lib().kvc_query_launch_ex(int(num_outputs), int(compress_ratio), int(state_dtype),
+                                   int(flags), ctypes.byref(c), ctypes.byref(k),
+                                   ctypes.byref(t), ctypes.byref(s))
+    if st != KVC_OK:
+        raise KvcError(st, "kvc_query_launch_ex")
+    return c.value, k.value, t.value, s.value
+
+
 def kvc_get_device_error(stream: Optional[int] = None) -> int:
     """Synchronise `stream` (a cudaStream_t as int), read and clear the
     device error code."""
@@ -204,6 +222,25 @@ def kvc_compress(state_cache, num_state_blocks, token_to_req, positions, num_tok
         v(kv_slot_mapping), slot_mapping_len, v(kv_cache), num_kv_pages, block_size,
         compress_ratio, ctypes.c_float(rms_norm_eps), v(y_out), v(workspace),
         workspace_bytes, flags, v(stream)))
+
+
+def kvc_compress_strided(state_cache, state_dtype, num_state_blocks, state_block_stride,
+                         state_row_stride, token_to_req, positions, num_tokens,
+                         boundary_token_indices, num_outputs, block_table, num_reqs,
+                         max_blocks_per_req, block_table_row_stride, block_table_col_stride,
+                         rms_norm_weight, cos_sin_cache, num_positions, kv_slot_mapping,
+                         slot_mapping_len, kv_cache, num_kv_pages, block_size, compress_ratio,
+                         rms_norm_eps, y_out, workspace, workspace_bytes, flags, stream) -> int:
+    """The strided / fp32-state C entry point with raw integer pointers."""
+    v = ctypes.c_void_p
+    return int(lib().kvc_compress_strided(
+        v(state_cache), int(state_dtype), num_state_blocks, state_block_stride,
+        state_row_stride, v(token_to_req), v(positions), num_tokens,
+        v(boundary_token_indices), num_outputs, v(block_table), num_reqs, max_blocks_per_req,
+        block_table_row_stride, block_table_col_stride, v(rms_norm_weight), v(cos_sin_cache),
+        num_positions, v(kv_slot_mapping), slot_mapping_len, v(kv_cache), num_kv_pages,
+        int(block_size), int(compress_ratio), float(rms_norm_eps), v(y_out), v(workspace),
+        int(workspace_bytes), int(flags), v(stream)))
 
 
 def kvc_compress_static(state_cache, num_state_blocks, token_to_req, positions, num_tokens,
@@ -298,16 +335,17 @@ def workspace_for(device, stream_ptr: int, num_outputs: int):
     return ws
 
 
-def _check(t, name, dtype, device):
+def _check(t, name, dtype, device, contiguous=True):
     import torch
 
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != dtype:
-        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    dtypes = dtype if isinstance(dtype, tuple) else (dtype,)
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype {' or '.join(map(str, dtypes))}, got {t.dtype}")
     if t.device != device:
         raise ValueError(f"{name} must be on {device}, got {t.device}")
-    if not t.is_contiguous():
+    if contiguous and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
 
@@ -317,11 +355,14 @@ def c128_256_512_compress(state_cache, token_to_req, positions, boundary_token_i
                           y_out=None, flags: int = 0, stream=None, workspace=None):
     """Compress every boundary token's window into its kv_cache slot, in place.
 
-    state_cache bf16 [blocks, 8, 1024]; token_to_req int32 [T]; positions
-    int64 [T]; boundary_token_indices int64 [N]; block_table int32 [R, Lb];
-    rms_norm_weight fp32 [512]; cos_sin_cache fp32 [P, 64]; kv_slot_mapping
-    int64 [T] (or [N]); kv_cache uint8 [pages, 37376].  All on one CUDA
-    device.  Optional y_out fp32 [N, 512] receives the normalised vectors.
+    state_cache bf16 or fp32 [blocks, block_size, 1024] (any block and row
+    strides, columns contiguous); token_to_req int32 [T]; positions int64
+    [T]; boundary_token_indices int64 [N]; block_table int32 [R, Lb] (any
+    strides); rms_norm_weight fp32 [512]; cos_sin_cache fp32 [P, 64];
+    kv_slot_mapping int64 [T] (or [N]); kv_cache uint8 [pages, 37376].  All
+    on one CUDA device.  Optional y_out fp32 [N, 512] receives the
+    normalised vectors.  A contiguous bf16 state with a contiguous table goes
+    through kvc_compress, anything else through kvc_compress_strided.
     Returns kv_cache.
     """
     import torch
@@ -329,17 +370,19 @@ def c128_256_512_compress(state_cache, token_to_req, positions, boundary_token_i
     dev = state_cache.device
     if dev.type != "cuda":
         raise ValueError("state_cache must be a CUDA tensor (there is no CPU path)")
-    _check(state_cache, "state_cache", torch.bfloat16, dev)
+    _check(state_cache, "state_cache", (torch.bfloat16, torch.float32), dev, contiguous=False)
     _check(token_to_req, "token_to_req", torch.int32, dev)
     _check(positions, "positions", torch.int64, dev)
     _check(boundary_token_indices, "boundary_token_indices", torch.int64, dev)
-    _check(block_table, "block_table", torch.int32, dev)
+    _check(block_table, "block_table", torch.int32, dev, contiguous=False)
     _check(rms_norm_weight, "rms_norm_weight", torch.float32, dev)
     _check(cos_sin_cache, "cos_sin_cache", torch.float32, dev)
     _check(kv_slot_mapping, "kv_slot_mapping", torch.int64, dev)
     _check(kv_cache, "kv_cache", torch.uint8, dev)
     if state_cache.dim() != 3 or state_cache.shape[2] != 2 * HEAD_DIM:
         raise ValueError("state_cache must be [num_blocks, block_size, 1024]")
+    if state_cache.stride(2) != 1:
+        raise ValueError("state_cache columns must be contiguous (stride(2) == 1)")
     if state_cache.shape[1] != block_size:
         raise ValueError("state_cache.shape[1] must equal block_size")
     if block_table.dim() != 2 or cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != 64:
@@ -359,17 +402,33 @@ def c128_256_512_compress(state_cache, token_to_req, positions, boundary_token_i
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         sp = int(s.cuda_stream)
         ws = workspace if workspace is not None else workspace_for(dev, sp, N)
-        st = kvc_compress(
-            state_cache.data_ptr(), state_cache.shape[0], token_to_req.data_ptr(),
-            positions.data_ptr(), positions.numel(), boundary_token_indices.data_ptr(), N,
-            block_table.data_ptr(), block_table.shape[0], block_table.shape[1],
-            rms_norm_weight.data_ptr(), cos_sin_cache.data_ptr(), cos_sin_cache.shape[0],
-            kv_slot_mapping.data_ptr(), kv_slot_mapping.numel(), kv_cache.data_ptr(),
-            kv_cache.shape[0], int(block_size), int(compress_ratio), float(rms_norm_eps),
-            0 if y_out is None else y_out.data_ptr(), ws.data_ptr(), ws.numel(),
-            int(flags), sp)
+        y_ptr = 0 if y_out is None else y_out.data_ptr()
+        if (state_cache.dtype == torch.bfloat16 and state_cache.is_contiguous()
+                and block_table.is_contiguous()):
+            name = "kvc_compress"
+            st = kvc_compress(
+                state_cache.data_ptr(), state_cache.shape[0], token_to_req.data_ptr(),
+                positions.data_ptr(), positions.numel(), boundary_token_indices.data_ptr(), N,
+                block_table.data_ptr(), block_table.shape[0], block_table.shape[1],
+                rms_norm_weight.data_ptr(), cos_sin_cache.data_ptr(), cos_sin_cache.shape[0],
+                kv_slot_mapping.data_ptr(), kv_slot_mapping.numel(), kv_cache.data_ptr(),
+                kv_cache.shape[0], int(block_size), int(compress_ratio), float(rms_norm_eps),
+                y_ptr, ws.data_ptr(), ws.numel(), int(flags), sp)
+        else:
+            name = "kvc_compress_strided"
+            st = kvc_compress_strided(
+                state_cache.data_ptr(),
+                KVC_DTYPE_F32 if state_cache.dtype == torch.float32 else KVC_DTYPE_BF16,
+                state_cache.shape[0], state_cache.stride(0), state_cache.stride(1),
+                token_to_req.data_ptr(), positions.data_ptr(), positions.numel(),
+                boundary_token_indices.data_ptr(), N, block_table.data_ptr(),
+                block_table.shape[0], block_table.shape[1], block_table.stride(0),
+                block_table.stride(1), rms_norm_weight.data_ptr(), cos_sin_cache.data_ptr(),
+                cos_sin_cache.shape[0], kv_slot_mapping.data_ptr(), kv_slot_mapping.numel(),
+                kv_cache.data_ptr(), kv_cache.shape[0], int(block_size), int(compress_ratio),
+                float(rms_norm_eps), y_ptr, ws.data_ptr(), ws.numel(), int(flags), sp)
     if st != KVC_OK:
-        raise KvcError(st, "kvc_compress")
+        raise KvcError(st, name)
     return kv_cache
 
 

@@ -68,6 +68,11 @@ kvc_status device_info(DeviceInfo* out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Bytes of one 8-row chunk of a state row type.
+double chunk_bytes_of(int32_t dtype) {
+  return static_cast<double>(kvc::kBlockRows) * kvc::kRowElems * (dtype == KVC_DTYPE_F32 ? 4 : 2);
+}
+
 struct Route {
   bool stream_k;
   int count;     // stream-K: CTAs; cluster route: clusters
@@ -89,12 +94,12 @@ int64_t balanced_clusters(int64_t N, int cap) {
   return (N + rounds - 1) / rounds;
 }
 
-// Cluster size for N outputs of K blocks: the estimated time of the slowest
-// CTA -- its blocks times the time one 16 KiB block takes when A CTAs share
-// the HBM (about 6.4 TB/s in all; one CTA's copy pipeline alone delivers
-// about 34 GB/s) -- plus about 1 us per cross-CTA merge.  Ties go to the
-// smaller cluster.  0 if no cluster size fits.
-int auto_cluster_size(const DeviceInfo& d, int64_t N, int64_t K) {
+// Cluster size for N outputs of K chunks of chunk_bytes each: the estimated
+// time of the slowest CTA -- its chunks times the time one chunk takes when
+// A CTAs share the HBM (about 6.4 TB/s in all; one CTA's copy pipeline alone
+// delivers about 34 GB/s) -- plus about 1 us per cross-CTA merge.  Ties go
+// to the smaller cluster.  0 if no cluster size fits.
+int auto_cluster_size(const DeviceInfo& d, int64_t N, int64_t K, double chunk_bytes) {
   constexpr double kTotalBytesPerUs = 6.4e6, kCtaBytesPerUs = 3.4e4, kMergeUs = 1.0;
   int best = 0;
   double best_t = 1e300;
@@ -106,7 +111,7 @@ int auto_cluster_size(const DeviceInfo& d, int64_t N, int64_t K) {
     const double kmax = static_cast<double>((K + S - 1) / S);
     const double A = static_cast<double>(ncl) * S;
     const double rate = kCtaBytesPerUs < kTotalBytesPerUs / A ? kCtaBytesPerUs : kTotalBytesPerUs / A;
-    const double t = rounds * kmax * kvc::kBlockBytes / rate + (S > 1 ? rounds * kMergeUs : 0.0);
+    const double t = rounds * kmax * chunk_bytes / rate + (S > 1 ? rounds * kMergeUs : 0.0);
     if (t < best_t * (1.0 - 1e-9)) {
       best_t = t;
       best = S;
@@ -115,16 +120,18 @@ int auto_cluster_size(const DeviceInfo& d, int64_t N, int64_t K) {
   return best;
 }
 
-// Route for N outputs of K chunks.  `aligned` = block_size 8 and C a multiple
-// of 8 (the stream-K route handles only those; the window start is checked
-// on the device).
-bool pick_route(const DeviceInfo& d, int64_t N, int64_t K, bool aligned, uint32_t flags,
-                Route* r) {
+// Route for N outputs of K chunks of chunk_bytes.  `streamk_ok` = a bf16
+// state with adjacent rows, block_size 8 and C a multiple of 8 (the stream-K
+// route handles only those; the window start is checked on the device).
+bool pick_route(const DeviceInfo& d, int64_t N, int64_t K, bool streamk_ok, double chunk_bytes,
+                uint32_t flags, Route* r) {
   const int forced_count = static_cast<int>(flags & KVC_FLAG_GRID_MASK);
   const int forced_s = static_cast<int>((flags & KVC_FLAG_CLUSTER_MASK) >> KVC_FLAG_CLUSTER_SHIFT);
-  const int S = (flags & KVC_FLAG_STREAM_K) ? 0 : (forced_s ? forced_s : auto_cluster_size(d, N, K));
+  const int S = (flags & KVC_FLAG_STREAM_K)
+                    ? 0
+                    : (forced_s ? forced_s : auto_cluster_size(d, N, K, chunk_bytes));
   if (S == 0) {  // stream-K: asked for, or no cluster size fits this device
-    if (!aligned) return false;
+    if (!streamk_ok) return false;
     const int64_t units = N * K;
     const int64_t cap = static_cast<int64_t>(d.sms) * d.streamk_ctas_per_sm;
     int64_t g = forced_count ? forced_count : cap;
@@ -152,18 +159,21 @@ size_t kvc_workspace_bytes(int64_t num_outputs) {
   return kvc::workspace_layout(d.sms * d.streamk_ctas_per_sm, num_outputs).total;
 }
 
-kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio, uint32_t flags,
-                            int32_t* ctas, int32_t* cluster_size, int32_t* threads,
-                            int32_t* smem_bytes) {
-  if (num_outputs < 0 || compress_ratio <= 0 || (flags & ~KVC_FLAG_ALL) != 0)
+kvc_status kvc_query_launch_ex(int64_t num_outputs, int32_t compress_ratio,
+                               int32_t state_dtype, uint32_t flags, int32_t* ctas,
+                               int32_t* cluster_size, int32_t* threads, int32_t* smem_bytes) {
+  if (num_outputs < 0 || compress_ratio <= 0 || (flags & ~KVC_FLAG_ALL) != 0 ||
+      (state_dtype != KVC_DTYPE_BF16 && state_dtype != KVC_DTYPE_F32))
     return KVC_ERR_INVALID_ARG;
   DeviceInfo d;
   const kvc_status st = device_info(&d);
   if (st != KVC_OK) return st;
   Route r{false, 0, 1};
   const int64_t K = (compress_ratio + kvc::kBlockRows - 1) / kvc::kBlockRows;
+  const bool bf16 = state_dtype == KVC_DTYPE_BF16;
   if (num_outputs > 0 &&
-      !pick_route(d, num_outputs, K, compress_ratio % kvc::kBlockRows == 0, flags, &r))
+      !pick_route(d, num_outputs, K, bf16 && compress_ratio % kvc::kBlockRows == 0,
+                  chunk_bytes_of(state_dtype), flags, &r))
     return KVC_ERR_UNSUPPORTED;
   if (ctas) *ctas = num_outputs > 0 ? (r.stream_k ? r.count : r.count * r.cluster) : 0;
   if (cluster_size) *cluster_size = r.stream_k ? 0 : r.cluster;
@@ -174,13 +184,33 @@ kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio, uint32_
   return KVC_OK;
 }
 
+kvc_status kvc_query_launch(int64_t num_outputs, int32_t compress_ratio, uint32_t flags,
+                            int32_t* ctas, int32_t* cluster_size, int32_t* threads,
+                            int32_t* smem_bytes) {
+  return kvc_query_launch_ex(num_outputs, compress_ratio, KVC_DTYPE_BF16, flags, ctas,
+                             cluster_size, threads, smem_bytes);
+}
+
 }  // extern "C"
 
 namespace {
 
+// State element type and strides (elements), block-table strides.
+struct StateLayout {
+  int32_t dtype;
+  int64_t block_stride, row_stride;
+  int64_t bt_row_stride, bt_col_stride;
+};
+
+StateLayout contiguous_layout(int32_t block_size, int64_t max_blocks_per_req) {
+  return StateLayout{KVC_DTYPE_BF16, static_cast<int64_t>(block_size) * kvc::kRowElems,
+                     kvc::kRowElems, max_blocks_per_req, 1};
+}
+
 // kvc_compress for L layers that share every index array: host arrays of L
 // device pointers for the state caches, weights and kv caches.
-kvc_status compress_layers(int32_t L, const void* const* state_caches, int64_t num_state_blocks,
+kvc_status compress_layers(int32_t L, const void* const* state_caches, const StateLayout& lay,
+                           int64_t num_state_blocks,
                            const int32_t* token_to_req, const int64_t* positions,
                            int64_t num_tokens, const int64_t* boundary_token_indices,
                            int64_t num_outputs, const int32_t* block_table, int64_t num_reqs,
@@ -192,6 +222,12 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, int64_t n
                            void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
   if (num_outputs < 0 || (flags & ~KVC_FLAG_ALL) != 0) return KVC_ERR_INVALID_ARG;
   if (L < 1 || L > kvc::kMaxLayers) return KVC_ERR_INVALID_ARG;
+  if (lay.dtype != KVC_DTYPE_BF16 && lay.dtype != KVC_DTYPE_F32) return KVC_ERR_INVALID_ARG;
+  if (lay.block_stride < 0 || lay.row_stride < 0 || lay.bt_row_stride < 0 || lay.bt_col_stride < 0)
+    return KVC_ERR_INVALID_ARG;
+  const int64_t esize = lay.dtype == KVC_DTYPE_F32 ? 4 : 2;
+  if ((lay.block_stride * esize) % 16 != 0 || (lay.row_stride * esize) % 16 != 0)
+    return KVC_ERR_UNSUPPORTED;
   if (block_size < kvc::kBlockRows) return KVC_ERR_UNSUPPORTED;
   if (compress_ratio <= 0) return KVC_ERR_INVALID_ARG;
   if (!std::isfinite(rms_norm_eps) || rms_norm_eps < 0.f) return KVC_ERR_INVALID_ARG;
@@ -210,6 +246,12 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, int64_t n
       num_positions <= 0 || num_kv_pages <= 0)
     return KVC_ERR_INVALID_ARG;
   if (slot_mapping_len != num_tokens && slot_mapping_len != num_outputs) return KVC_ERR_INVALID_ARG;
+  // every byte offset the kernels form must fit in int64
+  const __int128 state_end = static_cast<__int128>(lay.block_stride) * (num_state_blocks - 1) +
+                             static_cast<__int128>(lay.row_stride) * (block_size - 1) + kvc::kRowElems;
+  const __int128 table_end = static_cast<__int128>(lay.bt_row_stride) * (num_reqs - 1) +
+                             static_cast<__int128>(lay.bt_col_stride) * (max_blocks_per_req - 1);
+  if (state_end * esize > INT64_MAX || table_end > INT64_MAX / 4) return KVC_ERR_INVALID_ARG;
   if (!aligned(workspace, 16) || (y_out && !aligned(y_out, 8)) || !aligned(token_to_req, 4) ||
       !aligned(block_table, 4) || !aligned(cos_sin_cache, 4) || !aligned(positions, 8) ||
       !aligned(boundary_token_indices, 8) || !aligned(kv_slot_mapping, 8))
@@ -224,12 +266,16 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, int64_t n
 
   kvc::Params p = {};
   for (int l = 0; l < L; ++l) {
-    p.states[l] = static_cast<const uint16_t*>(state_caches[l]);
+    p.states[l] = static_cast<const uint8_t*>(state_caches[l]);
     p.weights[l] = rms_norm_weights[l];
     p.kvs[l] = kv_caches[l];
   }
   p.num_layers = L;
   p.num_blocks = num_state_blocks;
+  p.state_block_bytes = lay.block_stride * esize;
+  p.state_row_bytes = lay.row_stride * esize;
+  p.state_f32 = lay.dtype == KVC_DTYPE_F32 ? 1 : 0;
+  p.rows_contiguous = lay.row_stride == kvc::kRowElems ? 1 : 0;
   p.token_to_req = token_to_req;
   p.positions = positions;
   p.num_tokens = num_tokens;
@@ -238,6 +284,8 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, int64_t n
   p.block_table = block_table;
   p.num_reqs = num_reqs;
   p.max_blocks = max_blocks_per_req;
+  p.bt_row_stride = lay.bt_row_stride;
+  p.bt_col_stride = lay.bt_col_stride;
   p.cos_sin = cos_sin_cache;
   p.num_positions = num_positions;
   p.slot_map = kv_slot_mapping;
@@ -255,15 +303,18 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, int64_t n
   p.counters = reinterpret_cast<int32_t*>(ws + WL.counters);
   p.error = d.error_word;
 
-  const bool aligned8 = block_size == kvc::kBlockRows && compress_ratio % kvc::kBlockRows == 0;
+  const bool streamk_ok = lay.dtype == KVC_DTYPE_BF16 && p.rows_contiguous &&
+                          block_size == kvc::kBlockRows && compress_ratio % kvc::kBlockRows == 0;
+  const double chunk = chunk_bytes_of(lay.dtype);
   Route r;
-  if (!pick_route(d, num_outputs * L, p.blocks_per_output, aligned8, flags, &r))
+  if (!pick_route(d, num_outputs * L, p.blocks_per_output, streamk_ok, chunk, flags, &r))
     return KVC_ERR_UNSUPPORTED;
   p.cluster_size = r.cluster;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!r.stream_k) return kvc::launch_cluster(p, r.count, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
   // stream-K: one launch per layer (each reuses the workspace, in stream order)
-  const int ctas = pick_route(d, num_outputs, p.blocks_per_output, aligned8, flags, &r) ? r.count : 1;
+  const int ctas =
+      pick_route(d, num_outputs, p.blocks_per_output, streamk_ok, chunk, flags, &r) ? r.count : 1;
   for (int l = 0; l < L; ++l) {
     kvc::Params pl = p;
     pl.states[0] = p.states[l];
@@ -290,7 +341,8 @@ kvc_status kvc_compress(const void* state_cache, int64_t num_state_blocks,
                         int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
                         float* y_out, void* workspace, size_t workspace_bytes, uint32_t flags,
                         void* stream) {
-  return compress_layers(1, &state_cache, num_state_blocks, token_to_req, positions, num_tokens,
+  return compress_layers(1, &state_cache, contiguous_layout(block_size, max_blocks_per_req),
+                         num_state_blocks, token_to_req, positions, num_tokens,
                          boundary_token_indices, num_outputs, block_table, num_reqs,
                          max_blocks_per_req, &rms_norm_weight, cos_sin_cache, num_positions,
                          kv_slot_mapping, slot_mapping_len, &kv_cache, num_kv_pages, block_size,
@@ -310,10 +362,32 @@ kvc_status kvc_compress_layers(int32_t num_layers, const void* const* state_cach
                                int32_t compress_ratio, float rms_norm_eps, float* y_out,
                                void* workspace, size_t workspace_bytes, uint32_t flags,
                                void* stream) {
-  return compress_layers(num_layers, state_caches, num_state_blocks, token_to_req, positions,
+  return compress_layers(num_layers, state_caches,
+                         contiguous_layout(block_size, max_blocks_per_req), num_state_blocks,
+                         token_to_req, positions,
                          num_tokens, boundary_token_indices, num_outputs, block_table, num_reqs,
                          max_blocks_per_req, rms_norm_weights, cos_sin_cache, num_positions,
                          kv_slot_mapping, slot_mapping_len, kv_caches, num_kv_pages, block_size,
+                         compress_ratio, rms_norm_eps, y_out, workspace, workspace_bytes, flags,
+                         stream);
+}
+
+kvc_status kvc_compress_strided(
+    const void* state_cache, int32_t state_dtype, int64_t num_state_blocks,
+    int64_t state_block_stride, int64_t state_row_stride, const int32_t* token_to_req,
+    const int64_t* positions, int64_t num_tokens, const int64_t* boundary_token_indices,
+    int64_t num_outputs, const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    int64_t block_table_row_stride, int64_t block_table_col_stride, const float* rms_norm_weight,
+    const float* cos_sin_cache, int64_t num_positions, const int64_t* kv_slot_mapping,
+    int64_t slot_mapping_len, uint8_t* kv_cache, int64_t num_kv_pages, int32_t block_size,
+    int32_t compress_ratio, float rms_norm_eps, float* y_out, void* workspace,
+    size_t workspace_bytes, uint32_t flags, void* stream) {
+  const StateLayout lay{state_dtype, state_block_stride, state_row_stride, block_table_row_stride,
+                        block_table_col_stride};
+  return compress_layers(1, &state_cache, lay, num_state_blocks, token_to_req, positions,
+                         num_tokens, boundary_token_indices, num_outputs, block_table, num_reqs,
+                         max_blocks_per_req, &rms_norm_weight, cos_sin_cache, num_positions,
+                         kv_slot_mapping, slot_mapping_len, &kv_cache, num_kv_pages, block_size,
                          compress_ratio, rms_norm_eps, y_out, workspace, workspace_bytes, flags,
                          stream);
 }
@@ -366,8 +440,8 @@ const char* kvc_error_string(kvc_status status) {
 }
 
 const char* kvc_version(void) {
-  return "kvc 0.2.0 sm_103a: cluster route (S=1..16, bulk-copy ring 6x16KiB, st.async merges) "
-         "+ stream-K route";
+  return "kvc 0.3.0 sm_103a: cluster route (S=1..16, bf16/fp32 strided state, bulk-copy ring "
+         "96KiB, st.async merges) + stream-K route";
 }
 
 }  // extern "C"

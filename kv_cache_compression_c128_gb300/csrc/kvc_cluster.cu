@@ -9,9 +9,13 @@
 // Work decomposition.  A window of C rows is cut into K = ceil(C/8) chunks of
 // 8 rows (the last may be shorter); with the benchmark's block-aligned
 // windows and block_size 8 a chunk is exactly one 16 KiB physical block, in
-// general it is at most two runs of consecutive physical rows (block_size >=
-// 8).  Output n is handled by one thread-block cluster of S CTAs (S = 1, 2,
-// 4, 8, 16); rank j streams chunks [j K/S, (j+1) K/S).  Persistent clusters
+// general it is at most two runs of rows, each inside one physical block
+// (block_size >= 8).  The state is bf16 or fp32 ("The Baseline" sizes its
+// traffic with an fp32 element) and is addressed through block and row
+// strides ("A Bit of Triton and GPU Background"); the kernel is templated on
+// the element type, with a 16 KiB (bf16) or 32 KiB (fp32) chunk and the same
+// 96 KiB ring of 32 KiB stages either way.  Output n is handled by one thread-block cluster
+// of S CTAs (S = 1, 2, 4, 8, 16); rank j streams chunks [j K/S, (j+1) K/S).  Persistent clusters
 // take contiguous, equal ranges of outputs, so every CTA streams the same
 // number of chunks.  A multi-layer call simply has L * N outputs: output o is
 // window o mod N of layer o / N (same chunks, that layer's state cache,
@@ -22,8 +26,10 @@
 //   warp 9  resolver: turns units into physical blocks (boundary index ->
 //           request/position/slot -> block_table) 32 at a time, two chunks
 //           ahead, into a shared-memory FIFO;
-//   warp 8  issuer: one cp.async.bulk of 16 KiB per unit into a kStages ring,
-//           each stage guarded by a full/empty mbarrier pair;
+//   warp 8  issuer: one cp.async.bulk per run of rows (one per row when the
+//           rows of a block are not adjacent) into a ring of three 32 KiB
+//           stages (two bf16 chunks or one fp32 chunk each), each stage
+//           guarded by a full/empty mbarrier pair;
 //   warps 0-7 consumers: thread t owns dims 2t, 2t+1 and folds every staged
 //           block into its (max, denominator, numerator).
 // With S = 1 the consumers then finalise the output directly.  With S > 1
@@ -51,12 +57,26 @@ constexpr int kIssuerWarp = kConsumerWarps;
 constexpr int kResolverWarp = kConsumerWarps + 1;
 constexpr int kFifoChunk = 32;
 
+// Ring geometry of a state element type: a stage holds kChunksPerStage
+// consecutive 8-row chunks of one output (two 16 KiB bf16 chunks or one
+// 32 KiB fp32 chunk), so every stage is 32 KiB and the ring has 3 of them.
+template <bool F32>
+struct StateTraits {
+  static constexpr int kRowBytes = kRowElems * (F32 ? 4 : 2);
+  static constexpr int kChunkBytes = kBlockRows * kRowBytes;
+  static constexpr int kChunksPerStage = F32 ? 1 : 2;
+  static constexpr int kStageBytes = kChunksPerStage * kChunkBytes;
+  static constexpr int kNumStages = kRingBytes / kStageBytes;
+  static_assert(kNumStages >= 2 && kNumStages <= kStages, "ring geometry");
+  static_assert(kChunksPerStage * 8 <= 32, "rows of a stage's chunks are packed 8 bits each");
+};
+
 struct alignas(16) FifoEntry {
-  long long row1, row2;  // physical row runs of the chunk (row1 < 0: unresolved)
+  long long off1, off2;  // byte offsets of the chunk's row runs (off1 < 0: unresolved)
   long long slot;        // output slot (first unit of an output only)
   long long pc;          // compressed position (first unit of an output only)
   int n1, n2;            // rows in each run
-  int first;             // first unit of its output in this CTA
+  int kk;                // chunk index within this CTA's range of its output
   int piece;             // output index relative to the cluster's first output
   int layer;             // layer whose state cache the chunk is read from
   int pad_;
@@ -78,7 +98,7 @@ struct ClusterShared {
   float recv_bad[S > 1 ? S : 1];
   float ss_recv[kMaxFinalizers];
   FinalScratch fs;
-  uint32_t stage_rows[kStages];  // valid rows in each stage (0: unresolved chunk)
+  uint32_t stage_rows[kStages];  // valid rows of each chunk of a stage, 8 bits each (0: unresolved)
   int abort_flag;
 };
 
@@ -104,13 +124,13 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int6
       ChunkRuns cr;
       resolve_chunk(p, o - static_cast<int64_t>(layer) * p.num_outputs, k_lo + kk, kk == 0, cr, rec);
       e.layer = layer;
-      e.row1 = cr.row1;
-      e.row2 = cr.row2;
+      e.off1 = cr.off1;
+      e.off2 = cr.off2;
       e.n1 = cr.n1;
       e.n2 = cr.n2;
       e.slot = rec.slot;
       e.pc = rec.pc;
-      e.first = (kk == 0);
+      e.kk = kk;
       e.piece = static_cast<int>(q);
     }
     const int h = static_cast<int>(c & 1);
@@ -131,13 +151,16 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int6
   }
 }
 
-template <int S>
-__device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int64_t units) {
+template <int S, bool F32>
+__device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int64_t units, int kj) {
+  using T = StateTraits<F32>;
   if ((threadIdx.x & 31) != 0) return;
   const uint64_t policy = evict_first_policy();
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued = 0, last_parity = 0;
+  uint32_t rows_word = 0;  // rows of each chunk of the open stage, 8 bits per chunk
+  bool open = false;       // the current stage has copies announced but no arrival yet
   bool stop = false;
   for (int64_t c = 0; c * kFifoChunk < units && !stop; ++c) {
     const int h = static_cast<int>(c & 1);
@@ -152,49 +175,80 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
     const int64_t cnt = units - c * kFifoChunk < kFifoChunk ? units - c * kFifoChunk : kFifoChunk;
     for (int j = 0; j < cnt; ++j) {
       const FifoEntry e = sh.fifo[h][j];
-      if (aborted(&sh.abort_flag) || !mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u)) {
-        if (!aborted(&sh.abort_flag)) {
-          record_error(p.error, kErrTimeout);
-          set_abort(&sh.abort_flag);
+      const int half = e.kk % T::kChunksPerStage;  // which chunk of its stage
+      const bool closes = half == T::kChunksPerStage - 1 || e.kk == kj - 1;
+      if (half == 0) {
+        if (aborted(&sh.abort_flag) || !mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u)) {
+          if (!aborted(&sh.abort_flag)) {
+            record_error(p.error, kErrTimeout);
+            set_abort(&sh.abort_flag);
+          }
+          stop = true;
+          break;
         }
-        stop = true;
-        break;
+        rows_word = 0;
+        open = true;
       }
-      if (e.first) {
+      if (e.kk == 0) {
         MetaRec& m = sh.meta[e.piece % kMetaRing];
         m.slot = e.slot;
         m.pc = e.pc;
       }
-      if (e.row1 >= 0) {
-        constexpr uint32_t kRowBytes = kRowElems * 2;
-        uint8_t* dst = ring + static_cast<size_t>(stage) * kBlockBytes;
-        sh.stage_rows[stage] = static_cast<uint32_t>(e.n1 + e.n2);
-        mbar_arrive_expect_tx(&sh.full_bar[stage], (e.n1 + e.n2) * kRowBytes);
-        const uint16_t* state = p.states[e.layer];
-        bulk_copy_g2s(dst, state + e.row1 * kRowElems, e.n1 * kRowBytes, &sh.full_bar[stage], policy);
-        if (e.n2 > 0)
-          bulk_copy_g2s(dst + e.n1 * kRowBytes, state + e.row2 * kRowElems, e.n2 * kRowBytes,
-                        &sh.full_bar[stage], policy);
-      } else {
-        sh.stage_rows[stage] = 0;
+      if (e.off1 >= 0) {
+        constexpr uint32_t kRowBytes = T::kRowBytes;
+        uint8_t* dst = ring + static_cast<size_t>(stage) * T::kStageBytes +
+                       static_cast<size_t>(half) * T::kChunkBytes;
+        const int nr = e.n1 + e.n2;
+        rows_word |= static_cast<uint32_t>(nr) << (8 * half);
+        if (closes) {
+          sh.stage_rows[stage] = rows_word;
+          mbar_arrive_expect_tx(&sh.full_bar[stage], nr * kRowBytes);
+        } else {
+          mbar_expect_tx(&sh.full_bar[stage], nr * kRowBytes);
+        }
+        const uint8_t* state = p.states[e.layer];
+        if (p.rows_contiguous) {
+          bulk_copy_g2s(dst, state + e.off1, e.n1 * kRowBytes, &sh.full_bar[stage], policy);
+          if (e.n2 > 0)
+            bulk_copy_g2s(dst + e.n1 * kRowBytes, state + e.off2, e.n2 * kRowBytes,
+                          &sh.full_bar[stage], policy);
+        } else {
+          for (int i = 0; i < nr; ++i) {
+            const long long off = i < e.n1 ? e.off1 + i * p.state_row_bytes
+                                            : e.off2 + (i - e.n1) * p.state_row_bytes;
+            bulk_copy_g2s(dst + i * kRowBytes, state + off, kRowBytes, &sh.full_bar[stage], policy);
+          }
+        }
+      } else if (closes) {  // an unresolved chunk keeps 0 rows
+        sh.stage_rows[stage] = rows_word;
         mbar_arrive(&sh.full_bar[stage]);
       }
-      issued |= 1u << stage;
-      last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      if (closes) {
+        open = false;
+        issued |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == T::kNumStages) { stage = 0; phase ^= 1u; }
+      }
     }
     if (!stop) mbar_arrive(&sh.fifo_empty[h]);
   }
+  if (open) {  // abandoned between the chunks of a stage: close it so the drain can wait on it
+    sh.stage_rows[stage] = 0;
+    mbar_arrive(&sh.full_bar[stage]);
+    issued |= 1u << stage;
+    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+  }
   // No bulk copy may still target this CTA's shared memory when it exits.
-  for (int s = 0; s < kStages; ++s)
+  for (int s = 0; s < T::kNumStages; ++s)
     if ((issued >> s) & 1u)
       if (!mbar_wait_bounded(&sh.full_bar[s], (last_parity >> s) & 1u)) record_error(p.error, kErrTimeout);
 }
 
-template <int S>
+template <int S, bool F32>
 __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* ring, int64_t n0,
                           int64_t n1, int kj, uint32_t rank) {
   using Sh = ClusterShared<S>;
+  using T = StateTraits<F32>;
   constexpr int F = Sh::F, WD = Sh::WD;
   const int t = threadIdx.x, lane = t & 31;
   const bool finalizer = static_cast<int>(rank) < F;
@@ -218,7 +272,7 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
     bool bad = false;
     MetaRec meta{-1, -1};
     float cs = 1.f, sn = 0.f;
-    for (int kk = 0; kk < kj; ++kk) {
+    for (int kk = 0; kk < kj; kk += T::kChunksPerStage) {
       bool ready = false;
       if (!aborted(&sh.abort_flag)) {
         ready = mbar_wait_bounded(&sh.full_bar[stage], phase);
@@ -234,17 +288,26 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
           sn = __ldg(p.cos_sin + meta.pc * kRopeDim + kRopeDim / 2 + jp);
         }
       }
-      const uint32_t rows = ready ? sh.stage_rows[stage] : 0u;
-      if (rows == kBlockRows) {
-        fold_block(ring + static_cast<size_t>(stage) * kBlockBytes, t, s);
-      } else if (rows > 0) {
-        fold_rows(ring + static_cast<size_t>(stage) * kBlockBytes, t, s, static_cast<int>(rows));
-      } else {
-        bad = true;
+      const uint32_t word = ready ? sh.stage_rows[stage] : 0u;
+#pragma unroll
+      for (int c = 0; c < T::kChunksPerStage; ++c) {
+        if (kk + c >= kj) break;
+        const uint32_t rows = (word >> (8 * c)) & 0xFFu;
+        const uint8_t* chunk = ring + static_cast<size_t>(stage) * T::kStageBytes +
+                               static_cast<size_t>(c) * T::kChunkBytes;
+        if (rows == kBlockRows) {
+          if constexpr (F32) fold_f32<true>(chunk, t, s, kBlockRows);
+          else fold_block(chunk, t, s);
+        } else if (rows > 0) {
+          if constexpr (F32) fold_f32<false>(chunk, t, s, static_cast<int>(rows));
+          else fold_rows(chunk, t, s, static_cast<int>(rows));
+        } else {
+          bad = true;
+        }
       }
       __syncwarp();
       if (ready && lane == 0) mbar_arrive(&sh.empty_bar[stage]);
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      if (++stage == T::kNumStages) { stage = 0; phase ^= 1u; }
     }
 
     if constexpr (S == 1) {
@@ -321,11 +384,10 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
   }
 }
 
-template <int S>
+template <int S, bool F32>
 __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  ClusterShared<S>& sh =
-      *reinterpret_cast<ClusterShared<S>*>(smem + static_cast<size_t>(kStages) * kBlockBytes);
+  ClusterShared<S>& sh = *reinterpret_cast<ClusterShared<S>*>(smem + kRingBytes);
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
   const int64_t c = blockIdx.x / S, ncl = gridDim.x / S;
   const int64_t N = p.num_outputs * p.num_layers;  // outputs of all layers
@@ -362,9 +424,9 @@ __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const P
     if (warp == kResolverWarp) {
       resolver<S>(p, sh, n0, units, k_lo, kj);
     } else if (warp == kIssuerWarp) {
-      issuer<S>(p, sh, smem, units);
+      issuer<S, F32>(p, sh, smem, units, kj);
     } else {
-      consumers<S>(p, sh, smem, n0, n1, kj, rank);
+      consumers<S, F32>(p, sh, smem, n0, n1, kj, rank);
     }
   }
   if (S > 1) cluster_sync_all();  // no CTA leaves while a peer may still write to it
@@ -372,7 +434,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const P
 
 template <int S>
 size_t smem_bytes_of() {
-  return static_cast<size_t>(kStages) * kBlockBytes + sizeof(ClusterShared<S>);
+  return static_cast<size_t>(kRingBytes) + sizeof(ClusterShared<S>);
 }
 
 template <int S>
@@ -393,9 +455,9 @@ cudaLaunchConfig_t config_of(int clusters, cudaStream_t stream, cudaLaunchAttrib
   return cfg;
 }
 
-template <int S>
+template <int S, bool F32>
 int prepare_and_capacity() {
-  const void* fn = reinterpret_cast<const void*>(&kvc_cluster_kernel<S>);
+  const void* fn = reinterpret_cast<const void*>(&kvc_cluster_kernel<S, F32>);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes_of<S>())) != cudaSuccess)
     return 0;
@@ -405,15 +467,24 @@ int prepare_and_capacity() {
   cudaLaunchConfig_t cfg = config_of<S>(1, nullptr, attrs);
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, &kvc_cluster_kernel<S>, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, &kvc_cluster_kernel<S, F32>, &cfg) != cudaSuccess) return 0;
   return n;
+}
+
+// Both element types share the footprint; the capacity is the smaller one.
+template <int S>
+int prepare_and_capacity_both() {
+  const int a = prepare_and_capacity<S, false>();
+  const int b = prepare_and_capacity<S, true>();
+  return a < b ? a : b;
 }
 
 template <int S>
 cudaError_t launch_of(const Params& p, int clusters, cudaStream_t stream) {
   cudaLaunchAttribute attrs[2];
   cudaLaunchConfig_t cfg = config_of<S>(clusters, stream, attrs);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S>, p);
+  const cudaError_t e = p.state_f32 ? cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S, true>, p)
+                                    : cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S, false>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -435,11 +506,11 @@ size_t cluster_smem_bytes(int S) {
 int cluster_capacity(int S) {
   int n = 0;
   switch (S) {
-    case 1: n = prepare_and_capacity<1>(); break;
-    case 2: n = prepare_and_capacity<2>(); break;
-    case 4: n = prepare_and_capacity<4>(); break;
-    case 8: n = prepare_and_capacity<8>(); break;
-    case 16: n = prepare_and_capacity<16>(); break;
+    case 1: n = prepare_and_capacity_both<1>(); break;
+    case 2: n = prepare_and_capacity_both<2>(); break;
+    case 4: n = prepare_and_capacity_both<4>(); break;
+    case 8: n = prepare_and_capacity_both<8>(); break;
+    case 16: n = prepare_and_capacity_both<16>(); break;
   }
   (void)cudaGetLastError();  // a refused size leaves no sticky error behind
   return n;

@@ -55,6 +55,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, u
                : "memory");
 }
 
+// Raise the barrier's expected transaction bytes without arriving (a stage
+// filled by several copies announces each one; the last arrives).
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -313,7 +321,7 @@ __device__ __forceinline__ void resolve_unit(const Params& p, int64_t n, int k, 
   if (t0 & (kBlockRows - 1)) { record_error(p.error, kErrUnsupported); return; }
   const int64_t l = t0 / kBlockRows + k;
   if (l >= p.max_blocks) { record_error(p.error, kErrBadIndex); return; }
-  const int64_t g = __ldg(p.block_table + r * p.max_blocks + l);
+  const int64_t g = __ldg(p.block_table + r * p.bt_row_stride + l * p.bt_col_stride);
   if (g < 0 || g >= p.num_blocks) { record_error(p.error, kErrBadIndex); return; }
   blk = g;
   if (want_meta) {
@@ -330,20 +338,21 @@ __device__ __forceinline__ void resolve_unit(const Params& p, int64_t n, int k, 
 }
 
 // Rows of window chunk k (rows t0 + 8k .. t0 + 8k + nr - 1 of the request, nr
-// = min(8, C - 8k)) as at most two runs of consecutive physical rows: the
-// part in logical block l1 = (t0 + 8k) / B from offset o1, and the rest at the
-// start of block l1 + 1 (block_size B >= 8, so a chunk never touches three
-// blocks).  Row indices count rows of state_cache ([num_blocks * B, 1024]).
+// = min(8, C - 8k)) as at most two runs of rows that each lie in one
+// physical block: the part in logical block l1 = (t0 + 8k) / B from offset
+// o1, and the rest at the start of block l1 + 1 (block_size B >= 8, so a
+// chunk never touches three blocks).  Runs are given as byte offsets from
+// the state's base: block g, row o starts at g * block_bytes + o * row_bytes.
 struct ChunkRuns {
-  long long row1, row2;  // first physical row of each run (row1 < 0: bad chunk)
+  long long off1, off2;  // byte offset of each run's first row (off1 < 0: bad chunk)
   int n1, n2;            // rows in each run (n2 = 0: one run)
 };
 
 // Resolve chunk k of output n for the cluster route (any window start, any
-// C >= 1, any B >= 8), and, when want_meta, the output's slot and compressed
-// position.  All loads of one level are issued together: the chain before
-// the first copy is boundary index -> (request, position, slot) -> one or
-// two block-table entries.
+// C >= 1, any B >= 8, any state and block-table strides), and, when
+// want_meta, the output's slot and compressed position.  All loads of one
+// level are issued together: the chain before the first copy is boundary
+// index -> (request, position, slot) -> one or two block-table entries.
 __device__ __forceinline__ void resolve_chunk(const Params& p, int64_t n, int k, bool want_meta,
                                               ChunkRuns& cr, MetaRec& rec) {
   cr = ChunkRuns{-1, -1, 0, 0};
@@ -363,8 +372,9 @@ __device__ __forceinline__ void resolve_chunk(const Params& p, int64_t n, int k,
   const int n1 = static_cast<int>(B - o1 < nr ? B - o1 : nr);
   const int n2 = nr - n1;
   if (l1 + (n2 > 0 ? 1 : 0) >= p.max_blocks) { record_error(p.error, kErrBadIndex); return; }
-  const int64_t g1 = __ldg(p.block_table + r * p.max_blocks + l1);
-  const int64_t g2 = n2 > 0 ? __ldg(p.block_table + r * p.max_blocks + l1 + 1) : 0;
+  const int32_t* row = p.block_table + r * p.bt_row_stride;
+  const int64_t g1 = __ldg(row + l1 * p.bt_col_stride);
+  const int64_t g2 = n2 > 0 ? __ldg(row + (l1 + 1) * p.bt_col_stride) : 0;
   if (g1 < 0 || g1 >= p.num_blocks || g2 < 0 || g2 >= p.num_blocks) {
     record_error(p.error, kErrBadIndex);
     return;
@@ -378,9 +388,9 @@ __device__ __forceinline__ void resolve_chunk(const Params& p, int64_t n, int k,
     rec.slot = slot;
     rec.pc = pc;
   }
-  cr.row1 = g1 * B + o1;
+  cr.off1 = g1 * p.state_block_bytes + o1 * p.state_row_bytes;
   cr.n1 = n1;
-  cr.row2 = n2 > 0 ? g2 * B : -1;
+  cr.off2 = n2 > 0 ? g2 * p.state_block_bytes : -1;
   cr.n2 = n2;
 }
 
@@ -414,6 +424,50 @@ __device__ __forceinline__ void fold_rows(const uint8_t* blk, int t, SoftmaxStat
       a1 = fmaf(e1, bf16_hi(vw[r]), a1);
     }
   }
+  s.d0 = fmaf(s.d0, r0, d0);
+  s.d1 = fmaf(s.d1, r1, d1);
+  s.a0 = fmaf(s.a0, r0, a0);
+  s.a1 = fmaf(s.a1, r1, a1);
+  s.m0 = nm0;
+  s.m1 = nm1;
+}
+
+// fold_block / fold_rows for a staged fp32 chunk (8 rows x [512 values | 512
+// scores] fp32, 4 KiB per row): thread t reads float2 pairs of its dims.
+// With kFull the chunk holds all 8 rows; otherwise only its first `nrows`,
+// and the missing rows act as score -inf, value 0 (exp gives exactly 0).
+template <bool kFull>
+__device__ __forceinline__ void fold_f32(const uint8_t* blk, int t, SoftmaxState& s, int nrows) {
+  const float2* w = reinterpret_cast<const float2*>(blk);
+  float2 sw[kBlockRows], vw[kBlockRows];
+#pragma unroll
+  for (int r = 0; r < kBlockRows; ++r) {
+    const bool in = kFull || r < nrows;
+    sw[r] = in ? w[r * (kRowElems / 2) + (kHeadDim / 2) + t] : make_float2(-INFINITY, -INFINITY);
+    vw[r] = in ? w[r * (kRowElems / 2) + t] : make_float2(0.f, 0.f);
+  }
+  float mx0 = fmaxf(fmaxf(fmaxf(sw[0].x, sw[1].x), fmaxf(sw[2].x, sw[3].x)),
+                    fmaxf(fmaxf(sw[4].x, sw[5].x), fmaxf(sw[6].x, sw[7].x)));
+  float mx1 = fmaxf(fmaxf(fmaxf(sw[0].y, sw[1].y), fmaxf(sw[2].y, sw[3].y)),
+                    fmaxf(fmaxf(sw[4].y, sw[5].y), fmaxf(sw[6].y, sw[7].y)));
+  const float nm0 = fmaxf(s.m0, mx0);
+  const float nm1 = fmaxf(s.m1, mx1);
+  const float r0 = fast_ex2((s.m0 - nm0) * kLog2e);  // 0 on the first chunk
+  const float r1 = fast_ex2((s.m1 - nm1) * kLog2e);
+  const unsigned long long l2 = pack2(kLog2e, kLog2e);
+  const unsigned long long negmb = pack2(-nm0 * kLog2e, -nm1 * kLog2e);
+  unsigned long long dd = 0ull, aa = 0ull;
+#pragma unroll
+  for (int r = 0; r < kBlockRows; ++r) {
+    float x0, x1;
+    unpack2(fma2(pack2(sw[r].x, sw[r].y), l2, negmb), x0, x1);
+    const unsigned long long e = pack2(fast_ex2(x0), fast_ex2(x1));
+    dd = add2(dd, e);
+    aa = fma2(e, pack2(vw[r].x, vw[r].y), aa);
+  }
+  float d0, d1, a0, a1;
+  unpack2(dd, d0, d1);
+  unpack2(aa, a0, a1);
   s.d0 = fmaf(s.d0, r0, d0);
   s.d1 = fmaf(s.d1, r1, d1);
   s.a0 = fmaf(s.a0, r0, a0);

@@ -16,9 +16,9 @@ constexpr int kHeadDim = 512;
 constexpr int kNopeDim = 448;
 constexpr int kRopeDim = 64;
 constexpr int kGroup = 64;
-constexpr int kRowElems = 2 * kHeadDim;                    // bf16 per state row
-constexpr int kBlockRows = 8;                              // block_size
-constexpr int kBlockBytes = kBlockRows * kRowElems * 2;    // 16 KiB per block
+constexpr int kRowElems = 2 * kHeadDim;                    // elements per state row
+constexpr int kBlockRows = 8;                              // rows per chunk (block_size 8)
+constexpr int kBlockBytes = kBlockRows * kRowElems * 2;    // 16 KiB per bf16 chunk
 constexpr int kSlotsPerPage = 64;
 constexpr int kTokenStride = 576;
 constexpr int kScaleDim = 8;
@@ -32,7 +32,8 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
 constexpr int kMaxClusterSize = 16;
 constexpr int kMaxFinalizers = 8;
-constexpr int kStages = 6;                                 // 16 KiB ring stages
+constexpr int kStages = 6;                                 // 16 KiB ring stages (bf16)
+constexpr int kRingBytes = kStages * kBlockBytes;          // 96 KiB: 6 bf16 or 3 fp32 chunks
 constexpr int kMetaRing = kStages + 2;                     // per-output records
 
 // A split output's partial softmax state: m[512], den[512], num[512].
@@ -43,11 +44,15 @@ constexpr int kPartialFloats = 3 * kHeadDim;
 constexpr int kMaxLayers = 64;
 
 struct Params {
-  const uint16_t* states[kMaxLayers];  // per layer: bf16 bits [num_blocks, B, 1024]
+  const uint8_t* states[kMaxLayers];   // per layer: state base (bf16 or fp32 elements)
   const float* weights[kMaxLayers];    // per layer: rms_norm_weight [512]
   uint8_t* kvs[kMaxLayers];            // per layer: kv_cache [num_pages, 37376]
   int num_layers;                      // L; outputs of the call = L * num_outputs
   int64_t num_blocks;
+  int64_t state_block_bytes;           // bytes between physical blocks
+  int64_t state_row_bytes;             // bytes between rows of a block
+  int state_f32;                       // 1: fp32 elements, 0: bf16
+  int rows_contiguous;                 // state_row_bytes == one row's bytes
   const int32_t* token_to_req;
   const int64_t* positions;
   int64_t num_tokens;
@@ -56,6 +61,8 @@ struct Params {
   const int32_t* block_table;
   int64_t num_reqs;
   int64_t max_blocks;
+  int64_t bt_row_stride;          // block_table[r, l] at r * bt_row_stride + l * bt_col_stride
+  int64_t bt_col_stride;
   const float* cos_sin;
   int64_t num_positions;
   const int64_t* slot_map;
@@ -85,7 +92,8 @@ size_t streamk_smem_bytes();
 const void* streamk_kernel_symbol();
 cudaError_t launch_streamk(const Params& p, int ctas, cudaStream_t stream);
 
-// cluster route (kvc_cluster.cu); cluster sizes 1, 2, 4, 8, 16
+// cluster route (kvc_cluster.cu); cluster sizes 1, 2, 4, 8, 16; both state
+// dtypes use the same shared-memory footprint, so one capacity serves both
 int cluster_threads();
 size_t cluster_smem_bytes(int cluster_size);
 int cluster_capacity(int cluster_size);  // sets the kernel up; co-resident clusters (0: refused)

@@ -12,6 +12,8 @@
 // It needs no thread-block clusters; it is the route for devices or
 // configurations where the cluster route is unavailable, and it is the route
 // that uses scratch memory (the workspace, or the library's static buffer).
+// It takes a bf16 state whose 8-row blocks are 16 KiB contiguous (any block
+// stride, any block-table strides) and block-aligned windows.
 // One launch compresses one layer (the layer-0 pointers of its Params); the
 // host launches it once per layer of a multi-layer call.
 //
@@ -89,7 +91,7 @@ __device__ void producer(const Params& p, StreamKShared& sh, uint8_t* ring, int6
             sh.stage_ok[stage] = 1;
             mbar_arrive_expect_tx(&sh.full_bar[stage], kBlockBytes);
             bulk_copy_g2s(ring + static_cast<size_t>(stage) * kBlockBytes,
-                          p.states[0] + gb * (kBlockRows * kRowElems), kBlockBytes,
+                          p.states[0] + gb * p.state_block_bytes, kBlockBytes,
                           &sh.full_bar[stage], policy);
           } else {
             sh.stage_ok[stage] = 0;

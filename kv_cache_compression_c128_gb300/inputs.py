@@ -227,9 +227,10 @@ def embed_strided(state: np.ndarray, block_stride: int, row_stride: int,
     if fill is None:
         fill = np.uint16(0x7FC1) if state.dtype == np.uint16 else np.float32(np.nan)
     out = np.full(size, fill, dtype=state.dtype)
-    idx = (np.arange(G)[:, None, None] * block_stride + np.arange(B)[None, :, None] * row_stride
-           + np.arange(W)[None, None, :])
-    out[idx] = state
+    e = out.itemsize
+    view = np.lib.stride_tricks.as_strided(out, shape=(G, B, W),
+                                           strides=(block_stride * e, row_stride * e, e))
+    view[...] = state
     return out
 
 

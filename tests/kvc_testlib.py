@@ -130,13 +130,15 @@ def _y_ok(y_gpu, y_ref):
         (err / (np.abs(y_ref) + rms)).max())
 
 
-def assert_parity(oracle_mod, case, kv_g, y_g):
+def assert_parity(oracle_mod, case, kv_g, y_g, ref=None):
     """The three-way parity bar between GPU results (kv bytes, y) and the
     oracle on `case`: y within 2e-3 relative; kv bytes bit-exact against the
     oracle's finalizer applied to the GPU's y; against the oracle's own bytes
     within one quantisation step / one scale step / a bf16 ulp plus the y
-    tolerance, every other byte untouched.  Returns stats."""
-    kv_o, res = oracle_mod.compress_case(case)
+    tolerance, every other byte untouched.  `ref` = (kv, result dict) of an
+    oracle run already made (e.g. on an fp32 or strided state); default: the
+    oracle on the case's own bf16 state.  Returns stats."""
+    kv_o, res = oracle_mod.compress_case(case) if ref is None else ref
     assert res["status"] == 0
     ok, worst = _y_ok(y_g, res["y"])
     assert ok, f"y outside 2e-3 relative (worst scaled error {worst:.3g})"

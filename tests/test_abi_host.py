@@ -161,3 +161,55 @@ def test_layers_host_validation(kvc):
     assert kvc.kvc_compress_layers(**dict(base, state_caches=[0x10000, 0])) == 1
     assert kvc.kvc_compress_layers(**dict(base, kv_caches=[0x90000, 0x91004])) == 1
     assert kvc.kvc_compress_layers(**dict(base, num_outputs=0)) == 0
+
+
+def _strided_args(**change):
+    args = dict(_GOOD)
+    args.update(state_dtype=1, state_block_stride=8 * 1024, state_row_stride=1024,
+                block_table_row_stride=1024, block_table_col_stride=1)
+    args.update(change)
+    return args
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(state_dtype=2), 1),                       # unknown element type
+    (dict(state_dtype=-1), 1),
+    (dict(state_block_stride=-8), 1),
+    (dict(state_row_stride=-1024), 1),
+    (dict(block_table_row_stride=-1), 1),
+    (dict(block_table_col_stride=-1), 1),
+    (dict(state_row_stride=1028), 2),               # bf16: 2056 B, not a multiple of 16
+    (dict(state_block_stride=8 * 1024 + 4), 2),
+    (dict(state_dtype=0, state_row_stride=1026), 2),  # fp32: 4104 B
+    (dict(state_block_stride=1 << 62), 1),          # byte offsets overflow int64
+    (dict(block_table_row_stride=1 << 62, num_reqs=8), 1),
+    (dict(block_size=4), 2),
+    (dict(state_cache=0x10008), 1),
+])
+def test_strided_host_validation(kvc, change, status):
+    assert kvc.kvc_compress_strided(**_strided_args(**change)) == status
+
+
+def test_strided_zero_outputs_is_a_no_op(kvc):
+    assert kvc.kvc_compress_strided(**_strided_args(num_outputs=0)) == 0
+    assert kvc.kvc_compress_strided(**_strided_args(num_outputs=0, state_dtype=0)) == 0
+
+
+def test_query_launch_ex_rejects_bad_dtype(kvc):
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_query_launch_ex(64, 128, 5)
+
+
+def test_torch_wrapper_rejects_strided_columns(kvc):
+    import torch
+
+    from kv_cache_compression_c128_gb300 import inputs
+
+    case = inputs.make_case(1, 256, 16, seed=1)
+    st = torch.zeros((32, 1024, 8), dtype=torch.float32).transpose(1, 2)
+    t = torch.from_numpy
+    with pytest.raises(ValueError):
+        kvc.c128_256_512_compress(st, t(case.token_to_req), t(case.positions),
+                                  t(case.boundary_token_indices), t(case.block_table),
+                                  t(case.rms_norm_weight), t(case.cos_sin_cache),
+                                  t(case.kv_slot_mapping), t(case.kv_cache), 8, 16)
