@@ -95,10 +95,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", "kvc_compress_headline_traffic.json")
+def profiled_traffic(layout: str = "bf16"):
+    """DRAM bytes per launch from the committed ncu summary of the headline
+    workload in `layout`, if it was taken on the current kernel sources
+    (else None)."""
+    tag = "" if layout == "bf16" else f"_{layout}"
+    p = os.path.join(ROOT, "profiles", f"kvc_compress_headline{tag}_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -430,22 +432,27 @@ def bytes_for(case, n_outputs=None, elem_bytes: int = 2) -> int:
             + n * 584)
 
 
-def time_layouts(kvc, device, peak: float, steps: int = 600):
-    """The headline shape with the state in other layouts: fp32 elements
-    (contiguous), bf16 rows 64 elements apart (one bulk copy per row), and
-    bf16 blocks 512 elements apart with a column-major block table.  Each
-    layout is built on the device from the case's seeded values, three
-    rotating copies (> L2)."""
+# Other layouts of the headline state: name -> (bytes per element, kind).
+LAYOUTS = {
+    "bf16": (2, "contiguous bf16"),
+    "fp32_contiguous": (4, "fp32 elements (the seeded bf16 values widened), contiguous"),
+    "bf16_rows_64_apart": (2, "bf16 rows 1088 elements apart: one bulk copy per row"),
+    "bf16_blocks_512_apart_colmajor_table": (
+        2, "bf16 blocks 8*1024+512 elements apart, column-major block table"),
+}
+
+
+def layout_states(case, name, device, copies):
+    """`copies` device state tensors holding the case's values in layout
+    `name` (every element outside the rows is NaN), and the block table to
+    pass with them (None: the case's own row-major table)."""
     import torch
 
     from kv_cache_compression_c128_gb300 import inputs
 
-    case = inputs.headline_case()
     G, B = case.num_state_blocks, case.block_size
     R, M = case.block_table.shape
     bits = torch.from_numpy(case.state_bits.view(np.int16)).view(torch.bfloat16).to(device)
-    table_cm = torch.from_numpy(inputs.strided_table(case.block_table, 1, R)).to(device)
-    table_cm = table_cm.as_strided((R, M), (1, R))
 
     def embedded(src, rs, bs):
         size = (G - 1) * bs + (B - 1) * rs + 1024
@@ -454,15 +461,37 @@ def time_layouts(kvc, device, peak: float, steps: int = 600):
         view.copy_(src)
         return view
 
-    variants = [
-        ("fp32_contiguous", 4, lambda: bits.float(), None),
-        ("bf16_rows_64_apart", 2, lambda: embedded(bits, 1088, 8 * 1088), None),
-        ("bf16_blocks_512_apart_colmajor_table", 2, lambda: embedded(bits, 1024, 8 * 1024 + 512),
-         table_cm),
-    ]
+    table = None
+    if name == "bf16":
+        make = lambda: bits.clone()
+    elif name == "fp32_contiguous":
+        make = lambda: bits.float()
+    elif name == "bf16_rows_64_apart":
+        make = lambda: embedded(bits, 1088, 8 * 1088)
+    elif name == "bf16_blocks_512_apart_colmajor_table":
+        make = lambda: embedded(bits, 1024, 8 * 1024 + 512)
+        table = torch.from_numpy(inputs.strided_table(case.block_table, 1, R)).to(device)
+        table = table.as_strided((R, M), (1, R))
+    else:
+        raise ValueError(f"unknown state layout {name}")
+    states = [make() for _ in range(copies)]
+    del bits
+    return states, table
+
+
+def time_layouts(kvc, device, peak: float, steps: int = 600):
+    """The headline shape with the state in the other layouts of LAYOUTS
+    (fp32 elements; bf16 rows apart; padded bf16 blocks with a column-major
+    table), each built on the device from the case's seeded values, three
+    rotating copies (> L2)."""
+    from kv_cache_compression_c128_gb300 import inputs
+
+    case = inputs.headline_case()
     out = []
-    for name, eb, make, table in variants:
-        states = [make() for _ in range(3)]
+    for name, (eb, _) in LAYOUTS.items():
+        if name == "bf16":
+            continue
+        states, table = layout_states(case, name, device, 3)
         t, _ = time_device(kvc, case, device, steps, 20, states=states, block_table=table)
         b = bytes_for(case, elem_bytes=eb)
         dt = kvc.KVC_DTYPE_F32 if eb == 4 else kvc.KVC_DTYPE_BF16
@@ -482,9 +511,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
-    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="time the headline only: no shape sweep, reader, layers or layouts")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--state-layout", choices=sorted(LAYOUTS), default="bf16",
+                    help="layout of the timed headline state (default: contiguous bf16)")
     args = ap.parse_args()
     rank, world, local_rank = dist_env()
     from kv_cache_compression_c128_gb300 import inputs
@@ -512,23 +544,34 @@ def main():
     kvc.build()
     case = inputs.make_case(R, T, C, seed=rank_seed(inputs.BASE_SEED + inputs.BENCH_SHAPES.index(HEADLINE), rank),
                             name="headline")
-    per_call_bytes = bytes_for(case)
+    elem_bytes = LAYOUTS[args.state_layout][0]
+    per_call_bytes = bytes_for(case, elem_bytes=elem_bytes)
+    states = table = None
+    if args.state_layout != "bf16":
+        states, table = layout_states(case, args.state_layout, device,
+                                      max(3, -(-ROTATE_MIN_BYTES // (case.state_bits.nbytes
+                                                                   * elem_bytes // 2))))
     props = torch.cuda.get_device_properties(device)
     uuid = str(getattr(props, "uuid", "") or "")
     sampler = ClockSampler(uuid.replace("GPU-", "") if uuid else None)
     sampler.start()
     time.sleep(0.3)
-    t_call, t_total = time_device(kvc, case, device, args.steps, args.warmup, sampler)
+    t_call, t_total = time_device(kvc, case, device, args.steps, args.warmup, sampler,
+                                  states=states, block_table=table)
+    n_copies = len(states) if states is not None else _copies_for(case)
+    del states, table
     clocks = sampler.stop()
     t_max = max_over_ranks(t_total, device if world > 1 else None)
     ms_per_step = t_max / args.steps * 1e3
     value = world * per_call_bytes * args.steps / t_max / 1e9
     peak, peak_kind = measured_peaks()
     achieved = per_call_bytes / t_call / 1e9
-    ctas, cluster, threads, smem = kvc.kvc_query_launch(case.num_outputs, C)
+    f32 = elem_bytes == 4
+    ctas, cluster, threads, smem = kvc.kvc_query_launch_ex(
+        case.num_outputs, C, kvc.KVC_DTYPE_F32 if f32 else kvc.KVC_DTYPE_BF16)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.state_layout == "bf16":
         e_steps = max(3, min(50, args.steps))
         t_e2e, h2d, d2h = time_e2e(kvc, case, device, e_steps, 3)
         t_e2e = max_over_ranks(t_e2e, device if world > 1 else None)
@@ -536,9 +579,10 @@ def main():
                "us_per_call": round(t_e2e * 1e6, 2), "steps": e_steps,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    reader = time_reader(kvc, case, device) if rank == 0 else None
-    layers = time_layers(kvc, inputs.bench_case(0), device, 8) if rank == 0 else None
-    layouts = time_layouts(kvc, device, peak) if rank == 0 and not args.no_sweep else None
+    extras = rank == 0 and not args.no_sweep
+    reader = time_reader(kvc, case, device) if extras else None
+    layers = time_layers(kvc, inputs.bench_case(0), device, 8) if extras else None
+    layouts = time_layouts(kvc, device, peak) if extras else None
 
     sweep = None
     if not args.no_sweep and rank == 0:
@@ -570,20 +614,22 @@ def main():
 
     if rank != 0:
         return
-    traffic = profiled_traffic()
+    traffic = profiled_traffic(args.state_layout)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_call": round(ms_per_step * 1e3, 3),
         "pct_of_peak": round(100 * value / world / peak, 1),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if f32 else "bf16",
         "data": "synthetic: seeded N(0,1) bf16 state, random block permutation, "
                 "1+0.1N(0,1) weights, RoPE theta 10000, permuted slots",
         "config": {"workload": workload, "num_reqs": R, "total_tokens": T,
                    "compress_ratio": C, "block_size": 8, "outputs": case.num_outputs,
+                   "state_layout": f"{args.state_layout}: {LAYOUTS[args.state_layout][1]}",
                    "algorithmic_bytes_per_call": per_call_bytes,
-                   "l2": f"{_copies_for(case)} rotating state copies "
-                         f"({_copies_for(case) * case.state_bits.nbytes >> 20} MiB > L2)",
+                   "l2": f"{n_copies} rotating state copies "
+                         f"({n_copies * case.state_bits.nbytes * elem_bytes // 2 >> 20} MiB > L2)",
                    "timing": "CUDA graphs of <=250 launches, CUDA events on the launching stream",
                    "launch": {"ctas": ctas, "cluster_size": cluster, "threads": threads,
                               "smem_bytes": smem,
@@ -594,7 +640,8 @@ def main():
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": traffic,
-                     "kernel": f"kvc_cluster_kernel<{cluster}>" if cluster else "kvc_streamk_kernel",
+                     "kernel": (f"kvc_cluster_kernel<{cluster}, {'true' if f32 else 'false'}>"
+                                if cluster else "kvc_streamk_kernel"),
                      "algorithmic_bytes_per_launch": per_call_bytes},
         "gpu_launches": args.steps,
         "clocks": clocks,
