@@ -187,9 +187,10 @@ kvc_status kvc_compress_layers(
  *                     (both >= 0; e.g. 1 and num_reqs for a column-major
  *                     table), 4-byte aligned.
  * Everything else (arguments, results, errors, flags) as for kvc_compress.
- * The results are those of kvc_compress on the same values: the window sum
- * runs in fp32 over the elements as stored (bf16 widened exactly).  The
- * stream-K route takes only a bf16 state with adjacent rows.
+ * The results meet kvc_compress's bar on the same values: the window sum
+ * runs in fp32 over the elements as stored (bf16 widened exactly); only the
+ * order of the fp32 sums differs between element types.  The stream-K route
+ * takes only a bf16 state with adjacent rows.
  */
 kvc_status kvc_compress_strided(
     const void* state_cache, int32_t state_dtype, int64_t num_state_blocks,
@@ -286,6 +287,18 @@ kvc_status kvc_query_launch_ex(int64_t num_outputs, int32_t compress_ratio,
                                int32_t state_dtype, uint32_t flags, int32_t* ctas,
                                int32_t* cluster_size, int32_t* threads,
                                int32_t* smem_bytes);
+
+/*
+ * Self-test of the failure path that every pipeline wait of the kernels
+ * takes.  Launches one thread on `stream` that waits, through the same
+ * bounded mbarrier wait the kernels use, on a barrier nothing will ever
+ * complete, with a limit of limit_cycles SM clock cycles (1 .. 4e9; the
+ * kernels' own limit is 4e9, about 2 s).  The wait runs out, the thread
+ * records KVC_ERR_TIMEOUT in the device error word (read it with
+ * kvc_get_device_error) and returns: nothing traps or hangs, and the
+ * context stays usable.  KVC_ERR_INVALID_ARG for a limit outside the range.
+ */
+kvc_status kvc_selftest_wait_timeout(uint64_t limit_cycles, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device error code

@@ -24,7 +24,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(_LIB_DIR, "libkvc.so")
-_SOURCES = ["kvc_cluster.cu", "kvc_streamk.cu", "kvc_reader.cu", "kvc_api.cu", "kvc_static.cu"]
+_SOURCES = ["kvc_cluster.cu", "kvc_streamk.cu", "kvc_reader.cu", "kvc_api.cu", "kvc_static.cu",
+            "kvc_selftest.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 KVC_OK = 0
@@ -150,6 +151,8 @@ def lib():
             L.kvc_query_launch.restype = ctypes.c_int
             L.kvc_query_launch_ex.argtypes = [I64, I32, I32, U32, P, P, P, P]
             L.kvc_query_launch_ex.restype = ctypes.c_int
+            L.kvc_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
+            L.kvc_selftest_wait_timeout.restype = ctypes.c_int
             L.kvc_get_device_error.argtypes = [P, P]
             L.kvc_get_device_error.restype = ctypes.c_int
             L.kvc_error_string.argtypes = [ctypes.c_int]
@@ -195,6 +198,12 @@ def kvc_query_launch_ex(num_outputs: int, compress_ratio: int, state_dtype: int,
     if st != KVC_OK:
         raise KvcError(st, "kvc_query_launch_ex")
     return c.value, k.value, t.value, s.value
+
+
+def kvc_selftest_wait_timeout(limit_cycles: int, stream: Optional[int] = None) -> int:
+    """Launch the bounded-wait self-test (a wait that runs out after
+    limit_cycles and records KVC_ERR_TIMEOUT); returns the launch status."""
+    return int(lib().kvc_selftest_wait_timeout(int(limit_cycles), ctypes.c_void_p(stream or 0)))
 
 
 def kvc_get_device_error(stream: Optional[int] = None) -> int:

@@ -410,6 +410,16 @@ kvc_status kvc_dequantize(const uint8_t* kv_cache, int64_t num_kv_pages, const i
   return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
+kvc_status kvc_selftest_wait_timeout(uint64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > 4000000000ull) return KVC_ERR_INVALID_ARG;
+  DeviceInfo d;
+  const kvc_status st = device_info(&d);
+  if (st != KVC_OK) return st;
+  const cudaError_t e = kvc::launch_selftest_wait(static_cast<long long>(limit_cycles),
+                                                  d.error_word, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
 kvc_status kvc_get_device_error(void* stream, uint32_t* out_code) {
   if (out_code == nullptr) return KVC_ERR_INVALID_ARG;
   DeviceInfo d;

@@ -289,20 +289,26 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
         }
       }
       const uint32_t word = ready ? sh.stage_rows[stage] : 0u;
+      constexpr uint32_t kTwoFull = kBlockRows | (kBlockRows << 8);
+      if (!F32 && T::kChunksPerStage == 2 && kk + 1 < kj && word == kTwoFull) {
+        // two full chunks: 16 rows, 2 KiB apart, one shared rescale
+        fold_rows_n<2 * kBlockRows>(ring + static_cast<size_t>(stage) * T::kStageBytes, t, s);
+      } else {
 #pragma unroll
-      for (int c = 0; c < T::kChunksPerStage; ++c) {
-        if (kk + c >= kj) break;
-        const uint32_t rows = (word >> (8 * c)) & 0xFFu;
-        const uint8_t* chunk = ring + static_cast<size_t>(stage) * T::kStageBytes +
-                               static_cast<size_t>(c) * T::kChunkBytes;
-        if (rows == kBlockRows) {
-          if constexpr (F32) fold_f32<true>(chunk, t, s, kBlockRows);
-          else fold_block(chunk, t, s);
-        } else if (rows > 0) {
-          if constexpr (F32) fold_f32<false>(chunk, t, s, static_cast<int>(rows));
-          else fold_rows(chunk, t, s, static_cast<int>(rows));
-        } else {
-          bad = true;
+        for (int c = 0; c < T::kChunksPerStage; ++c) {
+          if (kk + c >= kj) break;
+          const uint32_t rows = (word >> (8 * c)) & 0xFFu;
+          const uint8_t* chunk = ring + static_cast<size_t>(stage) * T::kStageBytes +
+                                 static_cast<size_t>(c) * T::kChunkBytes;
+          if (rows == kBlockRows) {
+            if constexpr (F32) fold_f32<true>(chunk, t, s, kBlockRows);
+            else fold_block(chunk, t, s);
+          } else if (rows > 0) {
+            if constexpr (F32) fold_f32<false>(chunk, t, s, static_cast<int>(rows));
+            else fold_rows(chunk, t, s, static_cast<int>(rows));
+          } else {
+            bad = true;
+          }
         }
       }
       __syncwarp();

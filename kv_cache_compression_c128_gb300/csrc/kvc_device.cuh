@@ -75,15 +75,22 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
   return done != 0;
 }
 
-// Wait for the phase of `bar` with the given parity; false after the limit.
-static __device__ __noinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
+// Wait for the phase of `bar` with the given parity; false once more than
+// `limit` SM clock cycles have passed.
+static __device__ __noinline__ bool mbar_wait_bounded_for(unsigned long long* bar, uint32_t parity,
+                                                          long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
+}
+
+// The pipelines' wait: mbar_wait_bounded_for with the kernels' limit.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
+  return mbar_wait_bounded_for(bar, parity, kWaitLimitCycles);
 }
 
 // As mbar_wait_bounded, with cluster-scope acquire: for barriers completed by
@@ -259,35 +266,36 @@ __device__ __forceinline__ void state_reset(SoftmaxState& s) {
   s.d0 = s.d1 = s.a0 = s.a1 = 0.f;
 }
 
-// Fold one staged 8-row block (8 rows x [512 values | 512 scores] bf16) into
-// thread t's dimensions 2t, 2t+1: the block's score maximum (bf16x2, exact)
-// rescales the running state once, then every row adds exp(s - m) to the
-// denominator and exp(s - m) * v to the numerator (packed f32x2 arithmetic;
-// exp as ex2 of a log2e-scaled argument).
-__device__ __forceinline__ void fold_block(const uint8_t* blk, int t, SoftmaxState& s) {
+// Fold kRows consecutive staged rows (each [512 values | 512 scores] bf16,
+// 2 KiB apart) into thread t's dimensions 2t, 2t+1: the rows' score maximum
+// (bf16x2, exact) rescales the running state once, then every row adds
+// exp(s - m) to the denominator and exp(s - m) * v to the numerator (packed
+// f32x2 arithmetic; exp as ex2 of a log2e-scaled argument).  kRows = 8 is
+// one chunk; 16 is a stage of two full chunks, which share one rescale.
+template <int kRows>
+__device__ __forceinline__ void fold_rows_n(const uint8_t* blk, int t, SoftmaxState& s) {
   const uint32_t* w = reinterpret_cast<const uint32_t*>(blk);
-  uint32_t sw[kBlockRows], vw[kBlockRows];
+  uint32_t sw[kRows];
 #pragma unroll
-  for (int r = 0; r < kBlockRows; ++r) {
-    sw[r] = w[r * (kRowElems / 2) + (kHeadDim / 2) + t];
-    vw[r] = w[r * (kRowElems / 2) + t];
-  }
-  const uint32_t mx = bf16x2_max(bf16x2_max(bf16x2_max(sw[0], sw[1]), bf16x2_max(sw[2], sw[3])),
-                                 bf16x2_max(bf16x2_max(sw[4], sw[5]), bf16x2_max(sw[6], sw[7])));
+  for (int r = 0; r < kRows; ++r) sw[r] = w[r * (kRowElems / 2) + (kHeadDim / 2) + t];
+  uint32_t mx = sw[0];
+#pragma unroll
+  for (int r = 1; r < kRows; ++r) mx = bf16x2_max(mx, sw[r]);
   const float nm0 = fmaxf(s.m0, bf16_lo(mx));
   const float nm1 = fmaxf(s.m1, bf16_hi(mx));
-  const float r0 = fast_ex2((s.m0 - nm0) * kLog2e);  // 0 on the first block
+  const float r0 = fast_ex2((s.m0 - nm0) * kLog2e);  // 0 on the first rows
   const float r1 = fast_ex2((s.m1 - nm1) * kLog2e);
   const unsigned long long l2 = pack2(kLog2e, kLog2e);
   const unsigned long long negmb = pack2(-nm0 * kLog2e, -nm1 * kLog2e);
   unsigned long long dd = 0ull, aa = 0ull;
 #pragma unroll
-  for (int r = 0; r < kBlockRows; ++r) {
+  for (int r = 0; r < kRows; ++r) {
+    const uint32_t vw = w[r * (kRowElems / 2) + t];
     float x0, x1;
     unpack2(fma2(pack2(bf16_lo(sw[r]), bf16_hi(sw[r])), l2, negmb), x0, x1);
     const unsigned long long e = pack2(fast_ex2(x0), fast_ex2(x1));
     dd = add2(dd, e);
-    aa = fma2(e, pack2(bf16_lo(vw[r]), bf16_hi(vw[r])), aa);
+    aa = fma2(e, pack2(bf16_lo(vw), bf16_hi(vw)), aa);
   }
   float d0, d1, a0, a1;
   unpack2(dd, d0, d1);
@@ -298,6 +306,11 @@ __device__ __forceinline__ void fold_block(const uint8_t* blk, int t, SoftmaxSta
   s.a1 = fmaf(s.a1, r1, a1);
   s.m0 = nm0;
   s.m1 = nm1;
+}
+
+// One staged 8-row block.
+__device__ __forceinline__ void fold_block(const uint8_t* blk, int t, SoftmaxState& s) {
+  fold_rows_n<kBlockRows>(blk, t, s);
 }
 
 // ---- block table resolution -------------------------------------------------------

@@ -104,4 +104,7 @@ cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_
                               int64_t num_slots, void* out, int out_bf16, uint32_t* err,
                               cudaStream_t stream);
 
+// failure-path self-test (kvc_selftest.cu): one bounded wait that runs out
+cudaError_t launch_selftest_wait(long long limit_cycles, uint32_t* err, cudaStream_t stream);
+
 }  // namespace kvc

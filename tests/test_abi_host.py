@@ -213,3 +213,8 @@ def test_torch_wrapper_rejects_strided_columns(kvc):
                                   t(case.boundary_token_indices), t(case.block_table),
                                   t(case.rms_norm_weight), t(case.cos_sin_cache),
                                   t(case.kv_slot_mapping), t(case.kv_cache), 8, 16)
+
+
+def test_selftest_wait_rejects_bad_limits(kvc):
+    assert kvc.kvc_selftest_wait_timeout(0) == 1
+    assert kvc.kvc_selftest_wait_timeout(4_000_000_001) == 1
