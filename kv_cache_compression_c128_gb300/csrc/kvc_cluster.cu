@@ -151,10 +151,19 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int6
   }
 }
 
-template <int S, bool F32>
+// kSplitRows = false: rows of a block are adjacent; lane 0 alone walks the
+// FIFO and issues one copy per run of rows (the other lanes leave at once).
+// kSplitRows = true: rows are apart; the whole warp walks the FIFO (lane 0
+// waits, announces bytes and arrives) and the copies of a chunk are issued
+// one row per lane, so their issue does not serialise on one thread (measured
+// 67.2 -> 53.8 us at the headline with rows 64 elements apart, while the
+// warp-wide walk costs the adjacent-row case up to 1.5 %).
+template <int S, bool F32, bool kSplitRows>
 __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int64_t units, int kj) {
   using T = StateTraits<F32>;
-  if ((threadIdx.x & 31) != 0) return;
+  const int lane = threadIdx.x & 31;
+  if (!kSplitRows && lane != 0) return;
+  const auto lane0_says = [](bool v) { return kSplitRows ? __shfl_sync(0xffffffffu, v, 0) : v; };
   const uint64_t policy = evict_first_policy();
   int stage = 0;
   uint32_t phase = 0;
@@ -165,31 +174,37 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
   for (int64_t c = 0; c * kFifoChunk < units && !stop; ++c) {
     const int h = static_cast<int>(c & 1);
     const uint32_t ph = static_cast<uint32_t>((c >> 1) & 1);
-    if (aborted(&sh.abort_flag) || !mbar_wait_bounded(&sh.fifo_full[h], ph)) {
-      if (!aborted(&sh.abort_flag)) {
+    bool ok = true;
+    if (lane == 0) {
+      ok = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.fifo_full[h], ph);
+      if (!ok && !aborted(&sh.abort_flag)) {
         record_error(p.error, kErrTimeout);
         set_abort(&sh.abort_flag);
       }
-      break;
     }
+    if (!lane0_says(ok)) break;
     const int64_t cnt = units - c * kFifoChunk < kFifoChunk ? units - c * kFifoChunk : kFifoChunk;
     for (int j = 0; j < cnt; ++j) {
       const FifoEntry e = sh.fifo[h][j];
       const int half = e.kk % T::kChunksPerStage;  // which chunk of its stage
       const bool closes = half == T::kChunksPerStage - 1 || e.kk == kj - 1;
       if (half == 0) {
-        if (aborted(&sh.abort_flag) || !mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u)) {
-          if (!aborted(&sh.abort_flag)) {
+        bool free = true;
+        if (lane == 0) {
+          free = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u);
+          if (!free && !aborted(&sh.abort_flag)) {
             record_error(p.error, kErrTimeout);
             set_abort(&sh.abort_flag);
           }
+        }
+        if (!lane0_says(free)) {
           stop = true;
           break;
         }
         rows_word = 0;
         open = true;
       }
-      if (e.kk == 0) {
+      if (lane == 0 && e.kk == 0) {
         MetaRec& m = sh.meta[e.piece % kMetaRing];
         m.slot = e.slot;
         m.pc = e.pc;
@@ -200,26 +215,30 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
                        static_cast<size_t>(half) * T::kChunkBytes;
         const int nr = e.n1 + e.n2;
         rows_word |= static_cast<uint32_t>(nr) << (8 * half);
-        if (closes) {
-          sh.stage_rows[stage] = rows_word;
-          mbar_arrive_expect_tx(&sh.full_bar[stage], nr * kRowBytes);
-        } else {
-          mbar_expect_tx(&sh.full_bar[stage], nr * kRowBytes);
+        if (lane == 0) {
+          if (closes) {
+            sh.stage_rows[stage] = rows_word;
+            mbar_arrive_expect_tx(&sh.full_bar[stage], nr * kRowBytes);
+          } else {
+            mbar_expect_tx(&sh.full_bar[stage], nr * kRowBytes);
+          }
         }
         const uint8_t* state = p.states[e.layer];
-        if (p.rows_contiguous) {
+        if constexpr (!kSplitRows) {
           bulk_copy_g2s(dst, state + e.off1, e.n1 * kRowBytes, &sh.full_bar[stage], policy);
           if (e.n2 > 0)
             bulk_copy_g2s(dst + e.n1 * kRowBytes, state + e.off2, e.n2 * kRowBytes,
                           &sh.full_bar[stage], policy);
         } else {
-          for (int i = 0; i < nr; ++i) {
-            const long long off = i < e.n1 ? e.off1 + i * p.state_row_bytes
-                                            : e.off2 + (i - e.n1) * p.state_row_bytes;
-            bulk_copy_g2s(dst + i * kRowBytes, state + off, kRowBytes, &sh.full_bar[stage], policy);
+          __syncwarp();  // the bytes are announced before any row copy is issued
+          if (lane < nr) {
+            const long long off = lane < e.n1 ? e.off1 + lane * p.state_row_bytes
+                                              : e.off2 + (lane - e.n1) * p.state_row_bytes;
+            bulk_copy_g2s(dst + lane * kRowBytes, state + off, kRowBytes, &sh.full_bar[stage],
+                          policy);
           }
         }
-      } else if (closes) {  // an unresolved chunk keeps 0 rows
+      } else if (closes && lane == 0) {  // an unresolved chunk keeps 0 rows
         sh.stage_rows[stage] = rows_word;
         mbar_arrive(&sh.full_bar[stage]);
       }
@@ -230,8 +249,10 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
         if (++stage == T::kNumStages) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!stop) mbar_arrive(&sh.fifo_empty[h]);
+    if (kSplitRows) __syncwarp();  // every lane has read this FIFO half before it is handed back
+    if (!stop && lane == 0) mbar_arrive(&sh.fifo_empty[h]);
   }
+  if (lane != 0) return;
   if (open) {  // abandoned between the chunks of a stage: close it so the drain can wait on it
     sh.stage_rows[stage] = 0;
     mbar_arrive(&sh.full_bar[stage]);
@@ -430,7 +451,11 @@ __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const P
     if (warp == kResolverWarp) {
       resolver<S>(p, sh, n0, units, k_lo, kj);
     } else if (warp == kIssuerWarp) {
-      issuer<S, F32>(p, sh, smem, units, kj);
+      if (p.rows_contiguous) {
+        issuer<S, F32, false>(p, sh, smem, units, kj);
+      } else {
+        issuer<S, F32, true>(p, sh, smem, units, kj);
+      }
     } else {
       consumers<S, F32>(p, sh, smem, n0, n1, kj, rank);
     }
