@@ -13,7 +13,8 @@ with CUDA events on the launching stream, between device synchronisations
 (and a barrier plus max over ranks under torchrun).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--no-sweep] [--no-e2e] [--no-cpu]
+                  [--no-sweep] [--no-e2e] [--no-cpu] [--state-layout L]
+                  [--sweep-only]
 """
 from __future__ import annotations
 
@@ -21,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -274,6 +276,45 @@ def time_device(kvc, case, device, steps: int, warmup: int, sampler=None,
     return elapsed / steps, elapsed
 
 
+def time_distribution(kvc, case, device, iters: int = 200, warm: bool = False):
+    """Per-call device times (CUDA events around every call, no graph): the
+    median, p10 and p90 in microseconds.  Cold: the state rotates over
+    copies larger than L2 together; warm: one copy, read again and again.
+    A sleep kernel holds the stream while the host enqueues every call, so
+    the GPU never waits for the host between them and each event pair
+    brackets one kernel (the events also keep consecutive calls from
+    overlapping, unlike the graph-replayed headline)."""
+    import torch
+
+    copies = 1 if warm else _copies_for(case)
+    states, d = _tensors(case, device, copies)
+    ws = torch.zeros(kvc.kvc_workspace_bytes(case.num_outputs), dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            kvc.c128_256_512_compress(states[i % copies], block_size=case.block_size,
+                                      compress_ratio=case.compress_ratio,
+                                      rms_norm_eps=case.rms_norm_eps, stream=stream,
+                                      workspace=ws, **d)
+        stream.synchronize()
+        torch.cuda._sleep(150000 * iters)  # ~75 us of SM clock per queued call
+        for i in range(iters):
+            ev[i][0].record(stream)
+            kvc.c128_256_512_compress(states[i % copies], block_size=case.block_size,
+                                      compress_ratio=case.compress_ratio,
+                                      rms_norm_eps=case.rms_norm_eps, stream=stream,
+                                      workspace=ws, **d)
+            ev[i][1].record(stream)
+        stream.synchronize()
+    assert kvc.kvc_get_device_error(stream.cuda_stream) == 0
+    t = np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
+    return {"shape": case.name, "l2": "warm" if warm else "cold", "calls": iters,
+            "median_us": round(float(np.median(t)), 2), "p10_us": round(float(np.percentile(t, 10)), 2),
+            "p90_us": round(float(np.percentile(t, 90)), 2)}
+
+
 def time_reader(kvc, case, device, steps: int = 2000):
     """Per-call time of kvc_dequantize reading back every slot of `case`
     (fp32 and bf16 outputs), after one compression fills the cache."""
@@ -404,21 +445,27 @@ def time_e2e(kvc, case, device, steps: int, warmup: int):
     return elapsed / steps, h2d, d2h
 
 
-def time_oracle(case, max_outputs: int):
-    """Single-threaded oracle on the first `max_outputs` outputs of `case`."""
+def time_oracle(case, max_outputs: int, min_seconds: float = 0.0, max_passes: int = 1):
+    """Single-threaded oracle on the first `max_outputs` outputs of `case`,
+    repeated (up to max_passes) until min_seconds have passed.  Returns
+    (seconds, outputs computed in all passes)."""
     import oracle
 
     oracle.build()
     n = min(max_outputs, case.num_outputs)
-    kv = case.kv_cache.copy()
+    done = 0
     t0 = time.perf_counter()
-    res = oracle.compress(case.state_bits, case.token_to_req, case.positions,
-                          case.boundary_token_indices[:n], case.block_table,
-                          case.rms_norm_weight, case.cos_sin_cache, case.kv_slot_mapping, kv,
-                          case.block_size, case.compress_ratio, case.rms_norm_eps)
-    dt = time.perf_counter() - t0
-    assert res["status"] == 0
-    return dt, n
+    for _ in range(max(1, max_passes)):
+        kv = case.kv_cache.copy()
+        res = oracle.compress(case.state_bits, case.token_to_req, case.positions,
+                              case.boundary_token_indices[:n], case.block_table,
+                              case.rms_norm_weight, case.cos_sin_cache, case.kv_slot_mapping, kv,
+                              case.block_size, case.compress_ratio, case.rms_norm_eps)
+        assert res["status"] == 0
+        done += n
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    return time.perf_counter() - t0, done
 
 
 def bytes_for(case, n_outputs=None, elem_bytes: int = 2) -> int:
@@ -503,6 +550,29 @@ def time_layouts(kvc, device, peak: float, steps: int = 600):
     return out
 
 
+def run_sweep(kvc, inputs, device, peak: float, steps=None, warmup: int = 20):
+    """The 12 benchmark shapes, the 3 ragged variants and the general-window
+    headline, each timed like the headline (steps: 2000 for the small states,
+    600 for the large ones, unless given)."""
+    out = []
+    makers = ([lambda i=i: inputs.bench_case(i) for i in range(12)]
+              + [lambda c=c: inputs.ragged_case(c) for c in (128, 256, 512)]
+              + [lambda: inputs.general_window_case(128, 16), inputs.block16_case])
+    for make in makers:
+        cs = make()
+        n_steps = steps or (2000 if cs.state_bits.nbytes < 100 * 2 ** 20 else 600)
+        tc, _ = time_device(kvc, cs, device, n_steps, warmup)
+        b = bytes_for(cs)
+        sctas, sclu, _, _ = kvc.kvc_query_launch(cs.num_outputs, cs.compress_ratio)
+        out.append({"shape": cs.name, "outputs": cs.num_outputs, "bytes": b,
+                    "ctas": sctas, "cluster_size": sclu,
+                    "us_per_call": round(tc * 1e6, 3),
+                    "gb_s": round(b / tc / 1e9, 1),
+                    "pct_of_peak": round(100 * b / tc / 1e9 / peak, 1)})
+        del cs
+    return out
+
+
 # ---- main ------------------------------------------------------------------------
 
 def main():
@@ -515,6 +585,8 @@ def main():
                     help="time the headline only: no shape sweep, reader, layers or layouts")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="time only the shape sweep, --steps launches per shape (for ncu)")
     ap.add_argument("--state-layout", choices=sorted(LAYOUTS), default="bf16",
                     help="layout of the timed headline state (default: contiguous bf16)")
     args = ap.parse_args()
@@ -542,6 +614,11 @@ def main():
     import kv_cache_compression_c128_gb300 as kvc
 
     kvc.build()
+    if args.sweep_only:
+        peak, _ = measured_peaks()
+        print(json.dumps({"sweep": run_sweep(kvc, inputs, device, peak, args.steps,
+                                             args.warmup)}))
+        return
     case = inputs.make_case(R, T, C, seed=rank_seed(inputs.BASE_SEED + inputs.BENCH_SHAPES.index(HEADLINE), rank),
                             name="headline")
     elem_bytes = LAYOUTS[args.state_layout][0]
@@ -583,34 +660,23 @@ def main():
     reader = time_reader(kvc, case, device) if extras else None
     layers = time_layers(kvc, inputs.bench_case(0), device, 8) if extras else None
     layouts = time_layouts(kvc, device, peak) if extras else None
+    distribution = None
+    if extras:
+        small = inputs.bench_case(0)
+        distribution = [time_distribution(kvc, case, device), time_distribution(kvc, small, device),
+                        time_distribution(kvc, small, device, warm=True)]
 
-    sweep = None
-    if not args.no_sweep and rank == 0:
-        sweep = []
-        makers = ([lambda i=i: inputs.bench_case(i) for i in range(12)]
-                  + [lambda c=c: inputs.ragged_case(c) for c in (128, 256, 512)]
-                  + [lambda: inputs.general_window_case(128, 16)])
-        for make in makers:
-            cs = make()
-            n_steps = 2000 if cs.state_bits.nbytes < 100 * 2 ** 20 else 600
-            tc, _ = time_device(kvc, cs, device, n_steps, 20)
-            b = bytes_for(cs)
-            sctas, sclu, _, _ = kvc.kvc_query_launch(cs.num_outputs, cs.compress_ratio)
-            sweep.append({"shape": cs.name, "outputs": cs.num_outputs, "bytes": b,
-                          "ctas": sctas, "cluster_size": sclu,
-                          "us_per_call": round(tc * 1e6, 3),
-                          "gb_s": round(b / tc / 1e9, 1),
-                          "pct_of_peak": round(100 * b / tc / 1e9 / peak, 1)})
-            del cs
+    sweep = run_sweep(kvc, inputs, device, peak) if not args.no_sweep and rank == 0 else None
 
     cpu = None
     if not args.no_cpu and rank == 0 and world >= 1:
-        n_sample = case.num_outputs
-        dt, n = time_oracle(case, n_sample)
+        dt, n = time_oracle(case, case.num_outputs, min_seconds=10.0, max_passes=60)
         cpu = {"value": round(bytes_for(case, n) / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
                "kind": "oracle",
-               "sample": f"first {n} of the {case.num_outputs} outputs of the headline workload, "
-                         f"one pass, single-threaded C (float64 reduce), {dt:.2f} s"}
+               "sample": f"all {case.num_outputs} outputs of the headline workload, "
+                         f"{n // case.num_outputs} passes ({dt:.1f} s), single-threaded C "
+                         f"(float64 reduce) on one of {os.cpu_count()} "
+                         f"{platform.machine()} host cores"}
 
     if rank != 0:
         return
@@ -649,6 +715,7 @@ def main():
         "reader": reader,
         "layers": layers,
         "layouts": layouts,
+        "distribution": distribution,
         "cpu_baseline": cpu,
         "sweep": sweep,
         "kernel_source_hash": kernel_source_hash(),

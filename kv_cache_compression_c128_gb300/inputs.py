@@ -280,6 +280,13 @@ def general_window_case(compress_ratio: int = 128, block_size: int = 16) -> Case
                      name=f"general_r8_t131072_c{compress_ratio}_b{block_size}")
 
 
+def block16_case() -> Case:
+    """The headline shape (8 x 16384 tokens, C = 128, block-aligned windows)
+    with block_size 16: the same bytes in 32 KiB physical blocks."""
+    return make_case(8, 131072, 128, seed=BASE_SEED + 400, block_size=16,
+                     name="r8_t131072_c128_b16")
+
+
 def headline_case() -> Case:
     """8 requests x 16384 tokens, compress_ratio 128: the largest case."""
     return bench_case(BENCH_SHAPES.index((8, 131072, 128)))
