@@ -550,10 +550,14 @@ def time_layouts(kvc, device, peak: float, steps: int = 600):
     return out
 
 
-def run_sweep(kvc, inputs, device, peak: float, steps=None, warmup: int = 20):
-    """The 12 benchmark shapes, the 3 ragged variants and the general-window
-    headline, each timed like the headline (steps: 2000 for the small states,
-    600 for the large ones, unless given)."""
+def run_sweep(kvc, inputs, device, peak: float, steps=None, warmup: int = 20,
+              detail: bool = False):
+    """The 12 benchmark shapes, the 3 ragged variants, the general-window
+    headline and the headline with block_size 16, each timed like the
+    headline (steps: 2000 for the small states, 600 for the large ones,
+    unless given).  With `detail`, each shape also gets its per-call
+    distribution (100 calls, L2 cold and warm) and one single-threaded
+    oracle pass on the host."""
     out = []
     makers = ([lambda i=i: inputs.bench_case(i) for i in range(12)]
               + [lambda c=c: inputs.ragged_case(c) for c in (128, 256, 512)]
@@ -564,11 +568,19 @@ def run_sweep(kvc, inputs, device, peak: float, steps=None, warmup: int = 20):
         tc, _ = time_device(kvc, cs, device, n_steps, warmup)
         b = bytes_for(cs)
         sctas, sclu, _, _ = kvc.kvc_query_launch(cs.num_outputs, cs.compress_ratio)
-        out.append({"shape": cs.name, "outputs": cs.num_outputs, "bytes": b,
-                    "ctas": sctas, "cluster_size": sclu,
-                    "us_per_call": round(tc * 1e6, 3),
-                    "gb_s": round(b / tc / 1e9, 1),
-                    "pct_of_peak": round(100 * b / tc / 1e9 / peak, 1)})
+        row = {"shape": cs.name, "outputs": cs.num_outputs, "bytes": b,
+               "ctas": sctas, "cluster_size": sclu,
+               "us_per_call": round(tc * 1e6, 3),
+               "gb_s": round(b / tc / 1e9, 1),
+               "pct_of_peak": round(100 * b / tc / 1e9 / peak, 1)}
+        if detail:
+            cold = time_distribution(kvc, cs, device, 100)
+            warm = time_distribution(kvc, cs, device, 100, warm=True)
+            row["cold_us"] = {k: cold[k] for k in ("median_us", "p10_us", "p90_us")}
+            row["warm_us"] = {k: warm[k] for k in ("median_us", "p10_us", "p90_us")}
+            dt, _ = time_oracle(cs, cs.num_outputs)
+            row["oracle_ms_1_core"] = round(dt * 1e3, 1)
+        out.append(row)
         del cs
     return out
 
@@ -666,7 +678,8 @@ def main():
         distribution = [time_distribution(kvc, case, device), time_distribution(kvc, small, device),
                         time_distribution(kvc, small, device, warm=True)]
 
-    sweep = run_sweep(kvc, inputs, device, peak) if not args.no_sweep and rank == 0 else None
+    sweep = (run_sweep(kvc, inputs, device, peak, detail=not args.no_cpu)
+             if not args.no_sweep and rank == 0 else None)
 
     cpu = None
     if not args.no_cpu and rank == 0 and world >= 1:
