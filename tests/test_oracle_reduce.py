@@ -45,6 +45,21 @@ def test_reduce_matches_torch_softmax(oracle_mod, R, T, C):
     assert np.allclose(c, ref, rtol=2 ** -23, atol=1e-12)
 
 
+@pytest.mark.parametrize("R,T,C,B", [(2, 1536, 37, 24), (1, 1024, 5, 16), (2, 2048, 300, 32),
+                                     (3, 1536, 1, 8)])
+def test_general_windows_match_torch_softmax(oracle_mod, R, T, C, B):
+    # windows at random starts (not block aligned), block sizes other than 8
+    case = inputs.make_case(R, T, C, seed=200 + C + B, block_size=B, boundaries_per_req=30)
+    c = _reduce(oracle_mod, case)
+    rows = gather_window_rows(case)
+    st = bf16_bits_to_f32(case.state_bits.reshape(-1, 1024)).astype(np.float64)
+    all_rows = torch.from_numpy(st[rows.reshape(-1)]).reshape(rows.shape[0], C, 1024)
+    ref = (all_rows[..., :512] * torch.softmax(all_rows[..., 512:], dim=1)).sum(dim=1).numpy()
+    assert np.allclose(c, ref, rtol=2 ** -23, atol=1e-12)
+    starts = case.positions[case.boundary_token_indices] - C + 1
+    assert C == 1 or np.any(starts % B != 0)     # the case does exercise unaligned starts
+
+
 def _custom_case(C, T, v_fn, s_fn, R=1, seed=7):
     """A case whose state rows are set from token-level functions."""
     case = inputs.make_case(R, T, C, seed=seed)
