@@ -669,9 +669,20 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     extras = rank == 0 and not args.no_sweep
-    reader = time_reader(kvc, case, device) if extras else None
-    layers = time_layers(kvc, inputs.bench_case(0), device, 8) if extras else None
-    layouts = time_layouts(kvc, device, peak) if extras else None
+    # NVTX ranges name each part, so that ncu can capture one of them alone
+    # (--nvtx --nvtx-include "reader/")
+    nvtx = torch.cuda.nvtx
+    reader = layers = layouts = None
+    if extras:
+        nvtx.range_push("reader")
+        reader = time_reader(kvc, case, device)
+        nvtx.range_pop()
+        nvtx.range_push("layers")
+        layers = time_layers(kvc, inputs.bench_case(0), device, 8)
+        nvtx.range_pop()
+        nvtx.range_push("layouts")
+        layouts = time_layouts(kvc, device, peak)
+        nvtx.range_pop()
     distribution = None
     if extras:
         small = inputs.bench_case(0)
