@@ -293,6 +293,7 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
     bool bad = false;
     MetaRec meta{-1, -1};
     float cs = 1.f, sn = 0.f;
+    float2 w = make_float2(0.f, 0.f);  // RMSNorm weights of this thread's dims
     for (int kk = 0; kk < kj; kk += T::kChunksPerStage) {
       bool ready = false;
       if (!aborted(&sh.abort_flag)) {
@@ -303,6 +304,8 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
         }
       }
       if (kk == 0 && ready) {
+        // load what the finalise needs now, so its latency hides behind the window
+        if (active) w = __ldg(reinterpret_cast<const float2*>(p.weights[layer] + d0));
         meta = sh.meta[q % kMetaRing];
         if (rope && meta.pc >= 0) {
           cs = __ldg(p.cos_sin + meta.pc * kRopeDim + jp);
@@ -340,7 +343,7 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
     if constexpr (S == 1) {
       const float c0 = s.a0 / s.d0, c1 = s.a1 / s.d1;
       const float total = consumer_sum_squares(sh.fs, c0, c1);
-      finalize_slice(p, sh.fs, layer, o, true, 2 * t, c0, c1, bad, meta, cs, sn, total, 0, kHeadDim);
+      finalize_slice(p, sh.fs, layer, o, true, 2 * t, c0, c1, w, bad, meta, cs, sn, total, 0, kHeadDim);
     } else {
       // push this rank's partial state to the finaliser of each dim
       const uint32_t fbar = peer_addr(part_bar_l, f);
@@ -403,7 +406,8 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
         float total = 0.f;
 #pragma unroll
         for (int i = 0; i < F; ++i) total += sh.ss_recv[i];
-        finalize_slice(p, sh.fs, layer, o, active, d0, c0, c1, mbad, meta, cs, sn, total, dbase, WD);
+        finalize_slice(p, sh.fs, layer, o, active, d0, c0, c1, w, mbad, meta, cs, sn, total, dbase,
+                       WD);
       } else {
         consumer_sync();  // sh.fs.red is rewritten by the next output
       }

@@ -512,8 +512,9 @@ __device__ __forceinline__ float consumer_sum_squares(FinalScratch& fs, float c0
 // RMSNorm, NOPE quantisation, RoPE and the store of dims [dbase, dbase + wd)
 // of output row `row` (= layer * num_outputs + n: the y_out row) of layer
 // `layer`.  Thread t < wd/2 is `active` and owns dims d0 = dbase + 2t and
-// d0 + 1 with window sums c0, c1; `total` is the sum of c^2 over all 512
-// dims.  wd is a multiple of 64, so every 64-dim quantisation group lies in
+// d0 + 1 with window sums c0, c1 and RMSNorm weights w (loaded by the caller
+// ahead of time, so the load's latency is not spent here); `total` is the
+// sum of c^2 over all 512 dims.  wd is a multiple of 64, so every 64-dim quantisation group lies in
 // one warp and the RoPE dims 448..511 in the last.  The slice's bytes are
 // [dbase, dbase + wd) of the payload (up to 576 for the slice holding the
 // RoPE dims) and scale bytes [dbase/64, (dbase + wd)/64) (the last one is
@@ -521,13 +522,12 @@ __device__ __forceinline__ float consumer_sum_squares(FinalScratch& fs, float c0
 // consumer barriers).
 __device__ __forceinline__ void finalize_slice(const Params& p, FinalScratch& fs, int layer,
                                                int64_t row, bool active, int d0, float c0, float c1,
-                                               bool bad, const MetaRec& meta, float cs, float sn,
-                                               float total, int dbase, int wd) {
+                                               float2 w, bool bad, const MetaRec& meta, float cs,
+                                               float sn, float total, int dbase, int wd) {
   const int t = threadIdx.x, lane = t & 31;
   const bool invalid = consumer_any(bad) || meta.pc < 0;
   const float rho = __frsqrt_rn(total * (1.0f / kHeadDim) + p.eps);
   if (active) {
-    const float2 w = __ldg(reinterpret_cast<const float2*>(p.weights[layer] + d0));
     const float y0 = __fmul_rn(__fmul_rn(c0, rho), w.x);
     const float y1 = __fmul_rn(__fmul_rn(c1, rho), w.y);
     if (p.y_out != nullptr && !invalid)

@@ -118,8 +118,10 @@ __device__ void producer(const Params& p, StreamKShared& sh, uint8_t* ring, int6
 __device__ __forceinline__ void finalize_whole(const Params& p, StreamKShared& sh, int64_t n, float c0,
                                                float c1, bool bad, const MetaRec& meta, float cs,
                                                float sn) {
+  const float2 w = __ldg(reinterpret_cast<const float2*>(p.weights[0] + 2 * threadIdx.x));
   const float total = consumer_sum_squares(sh.fs, c0, c1);
-  finalize_slice(p, sh.fs, 0, n, true, 2 * threadIdx.x, c0, c1, bad, meta, cs, sn, total, 0, kHeadDim);
+  finalize_slice(p, sh.fs, 0, n, true, 2 * threadIdx.x, c0, c1, w, bad, meta, cs, sn, total, 0,
+                 kHeadDim);
 }
 
 // Store this CTA's partial state of output n; the last CTA to arrive merges
