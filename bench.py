@@ -211,10 +211,12 @@ def _copies_for(case) -> int:
 
 
 def time_device(kvc, case, device, steps: int, warmup: int, sampler=None,
-                graph_chunk: int = 250, states=None, block_table=None):
+                graph_chunk: int = 250, states=None, block_table=None, sync_ranks: bool = False):
     """Average seconds per call over `steps` graph-replayed launches.
     `states` (rotating state tensors, any layout) and `block_table` replace
-    the case's own contiguous bf16 state and table when given."""
+    the case's own contiguous bf16 state and table when given.  With
+    `sync_ranks` every rank must call it: the timed region starts and ends
+    with a barrier (the headline); rank-0-only measurements leave it off."""
     import torch
 
     if states is None:
@@ -259,7 +261,8 @@ def time_device(kvc, case, device, steps: int, warmup: int, sampler=None,
     with torch.cuda.stream(stream):
         graphs[0].replay()                    # warm the graph path itself
         torch.cuda.synchronize(device)
-        barrier()
+        if sync_ranks:
+            barrier()
         if sampler:
             sampler.mark(True)
         ev0.record(stream)
@@ -269,7 +272,8 @@ def time_device(kvc, case, device, steps: int, warmup: int, sampler=None,
         torch.cuda.synchronize(device)
     if sampler:
         sampler.mark(False)
-    barrier()
+    if sync_ranks:
+        barrier()
     elapsed = ev0.elapsed_time(ev1) / 1e3
     assert kvc.kvc_get_device_error(stream.cuda_stream) == 0
     del graphs
@@ -646,7 +650,7 @@ def main():
     sampler.start()
     time.sleep(0.3)
     t_call, t_total = time_device(kvc, case, device, args.steps, args.warmup, sampler,
-                                  states=states, block_table=table)
+                                  states=states, block_table=table, sync_ranks=True)
     n_copies = len(states) if states is not None else _copies_for(case)
     del states, table
     clocks = sampler.stop()
