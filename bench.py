@@ -629,6 +629,10 @@ def main():
     torch.cuda.set_device(device)
     import kv_cache_compression_c128_gb300 as kvc
 
+    # one rank compiles (if the library is out of date); the others then load it
+    if rank == 0:
+        kvc.build()
+    barrier()
     kvc.build()
     if args.sweep_only:
         peak, _ = measured_peaks()
