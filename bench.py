@@ -353,7 +353,41 @@ def time_reader(kvc, case, device, steps: int = 2000):
         b = M * (576 + 8 + 8) + M * 512 * width
         res[name] = {"us_per_call": round(t * 1e6, 3), "bytes": b, "gb_s": round(b / t / 1e9, 1)}
     assert kvc.kvc_get_device_error(torch.cuda.current_stream(device).cuda_stream) == 0
+    res["large"] = time_reader_large(kvc, device)
     return {"slots": M, **res}
+
+
+def time_reader_large(kvc, device, pages: int = 4096, reps: int = 20):
+    """kvc_dequantize over a 262144-slot cache (4096 pages of seeded random
+    bytes, 153 MB) read in a random slot order into fp32 and bf16 outputs:
+    the reader at a size where bandwidth, not launch latency, decides."""
+    import torch
+
+    gen = torch.Generator(device=device).manual_seed(20260614)
+    kv = torch.randint(0, 256, (pages, 64 * (576 + 8)), dtype=torch.uint8, device=device,
+                       generator=gen)
+    M = pages * 64
+    slots = torch.randperm(M, device=device, generator=gen)
+    res = {"slots": M}
+    stream = torch.cuda.Stream(device)
+    for name, dtype, width in (("f32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        out = torch.empty((M, 512), dtype=dtype, device=device)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                kvc.dequantize(kv, slots, dtype=dtype, out=out, stream=stream)
+            stream.synchronize()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(reps):
+                kvc.dequantize(kv, slots, dtype=dtype, out=out, stream=stream)
+            ev1.record(stream)
+            stream.synchronize()
+        t = ev0.elapsed_time(ev1) / 1e3 / reps
+        b = M * (576 + 8 + 8) + M * 512 * width
+        res[name] = {"us_per_call": round(t * 1e6, 2), "bytes": b, "gb_s": round(b / t / 1e9, 1)}
+        del out
+    assert kvc.kvc_get_device_error(stream.cuda_stream) == 0
+    return res
 
 
 def time_layers(kvc, case, device, L: int = 8, steps: int = 1000):

@@ -7,14 +7,17 @@
 // ("How One Output Is Produced") encodes: NOPE dim d < 448 reads back as
 // q_d * 2^(scale[d / 64] - 127), RoPE dims 448..511 as the stored bf16.
 //
-// One slot per 128 threads, 4 dims per thread: a thread reads 4 int8 codes
-// (or 4 bf16 RoPE values) and the group's scale byte, scales exactly with
-// ldexpf and writes one 16-byte (fp32) or 8-byte (bf16) vector.  Memory-bound:
-// 584 bytes read and 1 or 2 KiB written per slot.
+// Small calls: one slot per 128 threads, 4 dims per thread: a thread reads 4
+// int8 codes (or 4 bf16 RoPE values) and the group's scale byte, scales
+// exactly with ldexpf and writes one 16-byte (fp32) or 8-byte (bf16) vector.
+// Large calls (more slot pairs than fit on the device at once): one warp per
+// slot on a persistent grid, 4 slots per warp in flight, every load and
+// store coalesced.  584 bytes read and 1 or 2 KiB written per slot.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "kvc_internal.h"
@@ -27,44 +30,51 @@ constexpr int kThreadsPerSlot = kHeadDim / 4;   // 128
 constexpr int kSlotsPerCta = kReaderThreads / kThreadsPerSlot;
 constexpr uint32_t kErrBadIndexReader = 4;
 
-__global__ void __launch_bounds__(kReaderThreads) kvc_dequant_kernel(
-    const uint8_t* __restrict__ kv, int64_t num_pages, const int64_t* __restrict__ slots,
-    int64_t num_slots, void* __restrict__ out, int out_bf16, uint32_t* err) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t m = static_cast<int64_t>(blockIdx.x) * kSlotsPerCta + threadIdx.x / kThreadsPerSlot;
-  if (m >= num_slots) return;
-  const int t = threadIdx.x % kThreadsPerSlot;
-  const int d0 = 4 * t;
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
-  bool rope_bits = false;  // RoPE dims: the stored bf16 words, copied as they are
-  uint2 raw = make_uint2(0u, 0u);
-  const int64_t slot = __ldg(slots + m);
-  if (slot >= 0) {
-    const int64_t page = slot / kSlotsPerPage, off = slot % kSlotsPerPage;
-    if (page >= num_pages) {
-      if (t == 0) atomicCAS(err, 0u, kErrBadIndexReader);
-    } else {
-      const uint8_t* pg = kv + page * kPageBytes;
-      const uint8_t* payload = pg + off * kTokenStride;
-      if (d0 < kNopeDim) {
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(payload + d0));
-        const int e = static_cast<int>(__ldg(pg + kScaleBase + off * kScaleDim + d0 / kGroup)) - 127;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          v[i] = ldexpf(static_cast<float>(static_cast<int8_t>((w >> (8 * i)) & 0xFFu)), e);
-      } else {
-        raw = __ldg(reinterpret_cast<const uint2*>(payload + kNopeDim + 2 * (d0 - kNopeDim)));
-        rope_bits = true;
-        v[0] = __uint_as_float(raw.x << 16);
-        v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-        v[2] = __uint_as_float(raw.y << 16);
-        v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-      }
-    }
+// What one thread reads for its 4 dims of one slot.
+struct Piece {
+  uint32_t codes;  // 4 int8 codes (NOPE dims)
+  uint2 raw;       // 4 bf16 words (RoPE dims)
+  int e;           // the group's exponent
+  bool ok;         // the slot is read (non-negative and on a page)
+};
+
+__device__ __forceinline__ Piece load_piece(const uint8_t* __restrict__ kv, int64_t num_pages,
+                                            int64_t slot, int d0, int t, uint32_t* err) {
+  Piece pc{0u, make_uint2(0u, 0u), 0, false};
+  if (slot < 0) return pc;
+  const int64_t page = slot / kSlotsPerPage, off = slot % kSlotsPerPage;
+  if (page >= num_pages) {
+    if (t == 0) atomicCAS(err, 0u, kErrBadIndexReader);
+    return pc;
   }
-  if (out_bf16 && rope_bits) {
-    reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * kHeadDim)[t] = raw;
+  const uint8_t* pg = kv + page * kPageBytes;
+  const uint8_t* payload = pg + off * kTokenStride;
+  if (d0 < kNopeDim) {
+    pc.codes = __ldg(reinterpret_cast<const uint32_t*>(payload + d0));
+    pc.e = static_cast<int>(__ldg(pg + kScaleBase + off * kScaleDim + d0 / kGroup)) - 127;
+  } else {
+    pc.raw = __ldg(reinterpret_cast<const uint2*>(payload + kNopeDim + 2 * (d0 - kNopeDim)));
+  }
+  pc.ok = true;
+  return pc;
+}
+
+__device__ __forceinline__ void store_piece(const Piece& pc, int d0, int t, int64_t m, void* out,
+                                            int out_bf16) {
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  const bool rope = pc.ok && d0 >= kNopeDim;  // RoPE dims: the stored bf16 words, copied as they are
+  if (pc.ok && !rope) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      v[i] = ldexpf(static_cast<float>(static_cast<int8_t>((pc.codes >> (8 * i)) & 0xFFu)), pc.e);
+  } else if (rope) {
+    v[0] = __uint_as_float(pc.raw.x << 16);
+    v[1] = __uint_as_float(pc.raw.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(pc.raw.y << 16);
+    v[3] = __uint_as_float(pc.raw.y & 0xFFFF0000u);
+  }
+  if (out_bf16 && rope) {
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * kHeadDim)[t] = pc.raw;
   } else if (out_bf16) {
     uint2 o;
     o.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[0]))) |
@@ -78,13 +88,180 @@ __global__ void __launch_bounds__(kReaderThreads) kvc_dequant_kernel(
   }
 }
 
+// Grid-stride over the slots, kUnroll per 128-thread slot lane and pass: the
+// slot indices, then the codes and exponents of all kUnroll slots are loaded
+// before any is decoded and stored, so each thread keeps kUnroll chains in
+// flight, and at most a device-full of CTAs is launched.
+// kUnroll = 1 (the launcher's choice for calls of up to a device-full of
+// slot pairs): one slot per 128-thread lane.
+template <int kUnroll>
+__global__ void __launch_bounds__(kReaderThreads) kvc_dequant_kernel(
+    const uint8_t* __restrict__ kv, int64_t num_pages, const int64_t* __restrict__ slots,
+    int64_t num_slots, void* __restrict__ out, int out_bf16, uint32_t* err) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane_slot = threadIdx.x / kThreadsPerSlot;
+  const int t = threadIdx.x % kThreadsPerSlot;
+  const int d0 = 4 * t;
+  // the kUnroll slots of one pass lie one grid-width apart, so a grid with
+  // a CTA per two slots (small calls) gives every lane one slot, and the
+  // persistent grid of large calls gives every lane kUnroll per pass
+  const int64_t width = static_cast<int64_t>(gridDim.x) * kSlotsPerCta;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kSlotsPerCta + lane_slot;
+       base < num_slots; base += width * kUnroll) {
+    int64_t sl[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t m = base + u * width;
+      sl[u] = m < num_slots ? __ldg(slots + m) : -1;
+    }
+    Piece pc[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) pc[u] = load_piece(kv, num_pages, sl[u], d0, t, err);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t m = base + u * width;
+      if (m < num_slots) store_piece(pc[u], d0, t, m, out, out_bf16);
+    }
+  }
+}
+
+// One warp per slot: lane L handles dims 4L + 128k for k = 0..3, so every
+// load and store instruction of a warp covers one contiguous run of the slot
+// (128 code bytes, 512 fp32 or 256 bf16 output bytes).  Dims 0..447 are
+// NOPE; in pass k = 3, lanes 16..31 hold the RoPE dims 448..511.  The
+// slot's 8-byte scale record is read once per lane.  kUnroll slots per warp
+// and pass, one grid-width of warps apart, are loaded before any is written,
+// on a persistent grid: the large calls, where the bytes in flight per SM
+// decide the rate.
+template <int kUnroll>
+__global__ void __launch_bounds__(kReaderThreads) kvc_dequant_warp_kernel(
+    const uint8_t* __restrict__ kv, int64_t num_pages, const int64_t* __restrict__ slots,
+    int64_t num_slots, void* __restrict__ out, int out_bf16, uint32_t* err) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  constexpr int kWarps = kReaderThreads / 32;
+  const int lane = threadIdx.x & 31;
+  const bool rope_lane = lane >= 16;  // in pass 3
+  const int64_t width = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+       base < num_slots; base += width * kUnroll) {
+    int64_t sl[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t m = base + u * width;
+      sl[u] = m < num_slots ? __ldg(slots + m) : -1;
+    }
+    uint32_t codes[kUnroll][4];
+    uint2 scale[kUnroll], rope[kUnroll];
+    bool ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) codes[u][k] = 0u;
+      scale[u] = rope[u] = make_uint2(0u, 0u);
+      ok[u] = false;
+      if (sl[u] < 0) continue;
+      const int64_t page = sl[u] / kSlotsPerPage, off = sl[u] % kSlotsPerPage;
+      if (page >= num_pages) {
+        if (lane == 0) atomicCAS(err, 0u, kErrBadIndexReader);
+        continue;
+      }
+      const uint8_t* pg = kv + page * kPageBytes;
+      const uint8_t* payload = pg + off * kTokenStride;
+      scale[u] = __ldg(reinterpret_cast<const uint2*>(pg + kScaleBase + off * kScaleDim));
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        codes[u][k] = __ldg(reinterpret_cast<const uint32_t*>(payload + 4 * lane + 128 * k));
+      if (!rope_lane)
+        codes[u][3] = __ldg(reinterpret_cast<const uint32_t*>(payload + 4 * lane + 384));
+      else
+        rope[u] = __ldg(reinterpret_cast<const uint2*>(payload + kNopeDim + 8 * (lane - 16)));
+      ok[u] = true;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t m = base + u * width;
+      if (m >= num_slots) continue;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int d = 4 * lane + 128 * k;
+        const bool is_rope = k == 3 && rope_lane;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ok[u] && !is_rope) {
+          const int g = d / kGroup;  // 2k + lane / 16
+          const uint32_t sw = g < 4 ? scale[u].x : scale[u].y;
+          const int e = static_cast<int>((sw >> (8 * (g & 3))) & 0xFFu) - 127;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            v[i] = ldexpf(static_cast<float>(static_cast<int8_t>((codes[u][k] >> (8 * i)) & 0xFFu)), e);
+        } else if (is_rope) {
+          v[0] = __uint_as_float(rope[u].x << 16);
+          v[1] = __uint_as_float(rope[u].x & 0xFFFF0000u);
+          v[2] = __uint_as_float(rope[u].y << 16);
+          v[3] = __uint_as_float(rope[u].y & 0xFFFF0000u);
+        }
+        if (out_bf16) {
+          uint2 o;
+          if (is_rope) {  // the stored bf16 words, copied as they are
+            o = rope[u];
+          } else {
+            o.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[0]))) |
+                  (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[1]))) << 16);
+            o.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2]))) |
+                  (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[3]))) << 16);
+          }
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * kHeadDim + d) = o;
+        } else {
+          *reinterpret_cast<float4*>(static_cast<float*>(out) + m * kHeadDim + d) =
+              make_float4(v[0], v[1], v[2], v[3]);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+namespace {
+
+constexpr int kWideUnroll = 4;  // slots per warp and pass in the large-call kernel
+
+// CTAs of a kernel that fit on the current device at once (cached per device).
+int resident_ctas(int dev, const void* kernel, std::atomic<int>* cache) {
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kReaderThreads, 0) !=
+            cudaSuccess)
+      return 0;
+    n = sms * (per_sm > 0 ? per_sm : 1);
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_t* slots,
                               int64_t num_slots, void* out, int out_bf16, uint32_t* err,
                               cudaStream_t stream) {
+  static std::atomic<int> small_cap[64], large_cap[64];  // per device, 0: not yet known
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const void* small_fn = reinterpret_cast<const void*>(&kvc_dequant_kernel<1>);
+  const void* large_fn = reinterpret_cast<const void*>(&kvc_dequant_warp_kernel<kWideUnroll>);
+  const int cap_s = resident_ctas(dev, small_fn, small_cap);
+  const int cap_l = resident_ctas(dev, large_fn, large_cap);
+  if (cap_s == 0 || cap_l == 0) return cudaErrorInvalidDevice;
+  // up to a device-full of slot pairs: one CTA per pair, 128 threads per slot
+  // (the shortest chain); beyond that a persistent grid of warp-per-slot CTAs
+  const int64_t pairs = (num_slots + kSlotsPerCta - 1) / kSlotsPerCta;
+  const bool large = pairs > cap_s;
+  const int64_t warps8 = (num_slots + 7) / 8;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((num_slots + kSlotsPerCta - 1) / kSlotsPerCta));
+  cfg.gridDim = dim3(static_cast<unsigned>(large ? (warps8 < cap_l ? warps8 : cap_l) : pairs));
   cfg.blockDim = dim3(kReaderThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -92,8 +269,11 @@ cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, &kvc_dequant_kernel, kv, num_pages, slots, num_slots,
-                                           out, out_bf16, err);
+  const cudaError_t e =
+      large ? cudaLaunchKernelEx(&cfg, &kvc_dequant_warp_kernel<kWideUnroll>, kv, num_pages, slots,
+                                 num_slots, out, out_bf16, err)
+            : cudaLaunchKernelEx(&cfg, &kvc_dequant_kernel<1>, kv, num_pages, slots, num_slots, out,
+                                 out_bf16, err);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

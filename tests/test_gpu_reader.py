@@ -81,3 +81,28 @@ def test_reader_slot_beyond_last_page(kvc, oracle_mod):
     assert e == 4 and st == 4
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
     assert np.all(got[1:3] == 0)
+
+
+@pytest.mark.parametrize("M", [2433, 20011, 120000])
+def test_reader_large_calls_exact_on_random_bytes(kvc, oracle_mod, M):
+    # beyond a device-full of slot pairs the reader switches to its
+    # warp-per-slot persistent kernel; every byte pattern, slot order,
+    # negative slot, ragged tail and out-of-range slot must read back as the
+    # oracle's reader reads it
+    rng = np.random.default_rng(43 + M)
+    pages = 64
+    kv = rng.integers(0, 256, size=(pages, 37376), dtype=np.uint8)
+    slots = rng.integers(0, pages * 64, size=M).astype(np.int64)
+    slots[rng.choice(M, size=M // 50, replace=False)] = -1
+    for dtype, bf in ((torch.float32, False), (torch.bfloat16, True)):
+        got, e = _read(kvc, kv, slots, dtype)
+        want, st = oracle_mod.dequantize(kv, slots, out_bf16=bf)
+        assert e == 0 and st == 0
+        view = np.uint16 if bf else np.uint32
+        assert np.array_equal(got.view(view), want.view(view))
+    bad = slots.copy()
+    bad[M // 2] = pages * 64 + 5           # past the last page
+    got, e = _read(kvc, kv, bad, torch.float32)
+    want, st = oracle_mod.dequantize(kv, bad)
+    assert e == 4 and st == 4
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
