@@ -23,6 +23,7 @@ import hashlib
 import json
 import os
 import platform
+import re
 import subprocess
 import sys
 import threading
@@ -87,13 +88,21 @@ def measured_peaks():
 KERNEL_SOURCES = ("kvc_cluster.cu", "kvc_streamk.cu", "kvc_device.cuh", "kvc_internal.h")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed, so that a
+    comment edit does not orphan the ncu counters taken on the same code."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the fused kernel's sources (ties ncu counters to a kernel)."""
+    """Hash of the fused kernel's code (ties ncu counters to a kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_cache_compression_c128_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

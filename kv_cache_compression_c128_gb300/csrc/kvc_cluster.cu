@@ -14,10 +14,10 @@
 // traffic with an fp32 element) and is addressed through block and row
 // strides ("A Bit of Triton and GPU Background"); the kernel is templated on
 // the element type, with a 16 KiB (bf16) or 32 KiB (fp32) chunk and the same
-// 96 KiB ring of 32 KiB stages either way.  Output n is handled by one thread-block cluster
-// of S CTAs (S = 1, 2, 4, 8, 16); rank j streams chunks [j K/S, (j+1) K/S).  Persistent clusters
-// take contiguous, equal ranges of outputs, so every CTA streams the same
-// number of chunks.  A multi-layer call simply has L * N outputs: output o is
+// 96 KiB ring of 32 KiB stages either way.  Output n is handled by one
+// thread-block cluster of S CTAs (S = 1, 2, 4, 8, 16); rank j streams chunks
+// [j K/S, (j+1) K/S).  Persistent clusters take contiguous, equal ranges of
+// outputs, so every CTA streams the same number of chunks.  A multi-layer call simply has L * N outputs: output o is
 // window o mod N of layer o / N (same chunks, that layer's state cache,
 // weight and kv_cache), so all layers share one launch and one balanced
 // split.
@@ -31,7 +31,8 @@
 //           stages (two bf16 chunks or one fp32 chunk each), each stage
 //           guarded by a full/empty mbarrier pair;
 //   warps 0-7 consumers: thread t owns dims 2t, 2t+1 and folds every staged
-//           block into its (max, denominator, numerator).
+//           chunk into its (max, denominator, numerator), a stage of two
+//           full bf16 chunks as 16 rows with one rescale.
 // With S = 1 the consumers then finalise the output directly.  With S > 1
 // every rank pushes its partial state to the finaliser rank owning each dim
 // (F = min(S, 8) finalisers, 512/F dims each) with st.async, which completes
