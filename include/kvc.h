@@ -208,6 +208,28 @@ kvc_status kvc_compress_strided(
     uint32_t flags, void* stream);
 
 /*
+ * kvc_compress_layers over states of either element type at explicit
+ * strides, with a strided block table: the layout arguments of
+ * kvc_compress_strided (one layout shared by every layer), the per-layer
+ * pointer arrays of kvc_compress_layers.  Everything else, results and
+ * errors as for those two calls.
+ */
+kvc_status kvc_compress_layers_strided(
+    int32_t num_layers, const void* const* state_caches, int32_t state_dtype,
+    int64_t num_state_blocks, int64_t state_block_stride, int64_t state_row_stride,
+    const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
+    const int64_t* boundary_token_indices, int64_t num_outputs,
+    const int32_t* block_table, int64_t num_reqs, int64_t max_blocks_per_req,
+    int64_t block_table_row_stride, int64_t block_table_col_stride,
+    const float* const* rms_norm_weights,
+    const float* cos_sin_cache, int64_t num_positions,
+    const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+    uint8_t* const* kv_caches, int64_t num_kv_pages,
+    int32_t block_size, int32_t compress_ratio, float rms_norm_eps,
+    float* y_out, void* workspace, size_t workspace_bytes,
+    uint32_t flags, void* stream);
+
+/*
  * Read packed slots back as 512-vectors (the reader side of the cache: the
  * attention that consumes the compressed keys).  Layout of "Gather and
  * Scatter" in the write-up; values of its quantisation equation ("How One

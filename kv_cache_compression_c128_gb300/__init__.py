@@ -141,6 +141,10 @@ def lib():
                 I32, P, I64, P, P, I64, P, I64, P, I64, I64, P, P, I64, P, I64, P, I64,
                 I32, I32, ctypes.c_float, P, P, ctypes.c_size_t, U32, P]
             L.kvc_compress_layers.restype = ctypes.c_int
+            L.kvc_compress_layers_strided.argtypes = [
+                I32, P, I32, I64, I64, I64, P, P, I64, P, I64, P, I64, I64, I64, I64, P, P, I64,
+                P, I64, P, I64, I32, I32, ctypes.c_float, P, P, ctypes.c_size_t, U32, P]
+            L.kvc_compress_layers_strided.restype = ctypes.c_int
             L.kvc_dequantize.argtypes = [P, I64, P, I64, P, I32, P]
             L.kvc_dequantize.restype = ctypes.c_int
             L.kvc_compress_strided.argtypes = [
@@ -287,6 +291,28 @@ def kvc_compress_layers(num_layers, state_caches, num_state_blocks, token_to_req
         v(kv_slot_mapping), slot_mapping_len, arr(kv_caches), num_kv_pages, block_size,
         compress_ratio, ctypes.c_float(rms_norm_eps), v(y_out), v(workspace), workspace_bytes,
         flags, v(stream)))
+
+
+def kvc_compress_layers_strided(num_layers, state_caches, state_dtype, num_state_blocks,
+                                state_block_stride, state_row_stride, token_to_req, positions,
+                                num_tokens, boundary_token_indices, num_outputs, block_table,
+                                num_reqs, max_blocks_per_req, block_table_row_stride,
+                                block_table_col_stride, rms_norm_weights, cos_sin_cache,
+                                num_positions, kv_slot_mapping, slot_mapping_len, kv_caches,
+                                num_kv_pages, block_size, compress_ratio, rms_norm_eps, y_out,
+                                workspace, workspace_bytes, flags, stream) -> int:
+    """The strided multi-layer entry point (raw integer pointers, per-layer
+    sequences for the three per-layer arguments).  Returns the status."""
+    v = ctypes.c_void_p
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*[int(x) for x in xs])
+    return int(lib().kvc_compress_layers_strided(
+        int(num_layers), arr(state_caches), int(state_dtype), num_state_blocks,
+        state_block_stride, state_row_stride, v(token_to_req), v(positions), num_tokens,
+        v(boundary_token_indices), num_outputs, v(block_table), num_reqs, max_blocks_per_req,
+        block_table_row_stride, block_table_col_stride, arr(rms_norm_weights), v(cos_sin_cache),
+        num_positions, v(kv_slot_mapping), slot_mapping_len, arr(kv_caches), num_kv_pages,
+        int(block_size), int(compress_ratio), ctypes.c_float(rms_norm_eps), v(y_out),
+        v(workspace), int(workspace_bytes), int(flags), v(stream)))
 
 
 def kvc_dequantize(kv_cache, num_kv_pages, slots, num_slots, out, out_dtype, stream) -> int:
@@ -447,8 +473,11 @@ def compress_layers(state_caches, token_to_req, positions, boundary_token_indice
                     stream=None, workspace=None):
     """c128_256_512_compress for several layers in one launch: lists of
     per-layer state caches, RMSNorm weights and kv caches (same shapes and
-    dtypes as the single-layer call) sharing every index array.  y_out, if
-    given, is fp32 [L * N, 512] (layer-major).  Returns kv_caches."""
+    dtypes as the single-layer call) sharing every index array.  The state
+    caches are bf16 or fp32, all of one dtype and one set of strides (any
+    block and row strides, columns contiguous); the block table may have any
+    strides.  y_out, if given, is fp32 [L * N, 512] (layer-major).  Returns
+    kv_caches."""
     import torch
 
     L = len(state_caches)
@@ -457,18 +486,24 @@ def compress_layers(state_caches, token_to_req, positions, boundary_token_indice
     dev = state_caches[0].device
     if dev.type != "cuda":
         raise ValueError("state caches must be CUDA tensors (there is no CPU path)")
+    s0 = state_caches[0]
     for l in range(L):
-        _check(state_caches[l], f"state_caches[{l}]", torch.bfloat16, dev)
+        _check(state_caches[l], f"state_caches[{l}]", (torch.bfloat16, torch.float32), dev,
+               contiguous=False)
         _check(rms_norm_weights[l], f"rms_norm_weights[{l}]", torch.float32, dev)
         _check(kv_caches[l], f"kv_caches[{l}]", torch.uint8, dev)
-        if state_caches[l].shape != state_caches[0].shape or kv_caches[l].shape != kv_caches[0].shape:
+        if state_caches[l].shape != s0.shape or kv_caches[l].shape != kv_caches[0].shape:
             raise ValueError("all layers need the same state and kv_cache shapes")
+        if state_caches[l].dtype != s0.dtype or state_caches[l].stride() != s0.stride():
+            raise ValueError("all layers need the same state dtype and strides")
+    if s0.dim() != 3 or s0.shape[2] != 2 * HEAD_DIM or s0.stride(2) != 1:
+        raise ValueError("state caches must be [num_blocks, block_size, 1024] with contiguous columns")
     for name, t, dt in (("token_to_req", token_to_req, torch.int32), ("positions", positions, torch.int64),
                         ("boundary_token_indices", boundary_token_indices, torch.int64),
-                        ("block_table", block_table, torch.int32),
                         ("cos_sin_cache", cos_sin_cache, torch.float32),
                         ("kv_slot_mapping", kv_slot_mapping, torch.int64)):
         _check(t, name, dt, dev)
+    _check(block_table, "block_table", torch.int32, dev, contiguous=False)
     N = boundary_token_indices.numel()
     if y_out is not None:
         _check(y_out, "y_out", torch.float32, dev)
@@ -478,15 +513,31 @@ def compress_layers(state_caches, token_to_req, positions, boundary_token_indice
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         sp = int(s.cuda_stream)
         ws = workspace if workspace is not None else workspace_for(dev, sp, N)
-        st = kvc_compress_layers(
-            L, [t.data_ptr() for t in state_caches], state_caches[0].shape[0],
-            token_to_req.data_ptr(), positions.data_ptr(), positions.numel(),
-            boundary_token_indices.data_ptr(), N, block_table.data_ptr(), block_table.shape[0],
-            block_table.shape[1], [t.data_ptr() for t in rms_norm_weights],
-            cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], kv_slot_mapping.data_ptr(),
-            kv_slot_mapping.numel(), [t.data_ptr() for t in kv_caches], kv_caches[0].shape[0],
-            int(block_size), int(compress_ratio), float(rms_norm_eps),
-            0 if y_out is None else y_out.data_ptr(), ws.data_ptr(), ws.numel(), int(flags), sp)
+        y_ptr = 0 if y_out is None else y_out.data_ptr()
+        if s0.dtype == torch.bfloat16 and s0.is_contiguous() and block_table.is_contiguous():
+            name = "kvc_compress_layers"
+            st = kvc_compress_layers(
+                L, [t.data_ptr() for t in state_caches], s0.shape[0],
+                token_to_req.data_ptr(), positions.data_ptr(), positions.numel(),
+                boundary_token_indices.data_ptr(), N, block_table.data_ptr(), block_table.shape[0],
+                block_table.shape[1], [t.data_ptr() for t in rms_norm_weights],
+                cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], kv_slot_mapping.data_ptr(),
+                kv_slot_mapping.numel(), [t.data_ptr() for t in kv_caches], kv_caches[0].shape[0],
+                int(block_size), int(compress_ratio), float(rms_norm_eps), y_ptr, ws.data_ptr(),
+                ws.numel(), int(flags), sp)
+        else:
+            name = "kvc_compress_layers_strided"
+            st = kvc_compress_layers_strided(
+                L, [t.data_ptr() for t in state_caches],
+                KVC_DTYPE_F32 if s0.dtype == torch.float32 else KVC_DTYPE_BF16, s0.shape[0],
+                s0.stride(0), s0.stride(1), token_to_req.data_ptr(), positions.data_ptr(),
+                positions.numel(), boundary_token_indices.data_ptr(), N, block_table.data_ptr(),
+                block_table.shape[0], block_table.shape[1], block_table.stride(0),
+                block_table.stride(1), [t.data_ptr() for t in rms_norm_weights],
+                cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], kv_slot_mapping.data_ptr(),
+                kv_slot_mapping.numel(), [t.data_ptr() for t in kv_caches], kv_caches[0].shape[0],
+                int(block_size), int(compress_ratio), float(rms_norm_eps), y_ptr, ws.data_ptr(),
+                ws.numel(), int(flags), sp)
     if st != KVC_OK:
-        raise KvcError(st, "kvc_compress_layers")
+        raise KvcError(st, name)
     return kv_caches

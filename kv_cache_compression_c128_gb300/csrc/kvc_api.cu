@@ -392,6 +392,27 @@ kvc_status kvc_compress_strided(
                          stream);
 }
 
+kvc_status kvc_compress_layers_strided(
+    int32_t num_layers, const void* const* state_caches, int32_t state_dtype,
+    int64_t num_state_blocks, int64_t state_block_stride, int64_t state_row_stride,
+    const int32_t* token_to_req, const int64_t* positions, int64_t num_tokens,
+    const int64_t* boundary_token_indices, int64_t num_outputs, const int32_t* block_table,
+    int64_t num_reqs, int64_t max_blocks_per_req, int64_t block_table_row_stride,
+    int64_t block_table_col_stride, const float* const* rms_norm_weights,
+    const float* cos_sin_cache, int64_t num_positions, const int64_t* kv_slot_mapping,
+    int64_t slot_mapping_len, uint8_t* const* kv_caches, int64_t num_kv_pages, int32_t block_size,
+    int32_t compress_ratio, float rms_norm_eps, float* y_out, void* workspace,
+    size_t workspace_bytes, uint32_t flags, void* stream) {
+  const StateLayout lay{state_dtype, state_block_stride, state_row_stride, block_table_row_stride,
+                        block_table_col_stride};
+  return compress_layers(num_layers, state_caches, lay, num_state_blocks, token_to_req, positions,
+                         num_tokens, boundary_token_indices, num_outputs, block_table, num_reqs,
+                         max_blocks_per_req, rms_norm_weights, cos_sin_cache, num_positions,
+                         kv_slot_mapping, slot_mapping_len, kv_caches, num_kv_pages, block_size,
+                         compress_ratio, rms_norm_eps, y_out, workspace, workspace_bytes, flags,
+                         stream);
+}
+
 kvc_status kvc_dequantize(const uint8_t* kv_cache, int64_t num_kv_pages, const int64_t* slots,
                           int64_t num_slots, void* out, int32_t out_dtype, void* stream) {
   if (num_slots < 0 || (out_dtype != KVC_DTYPE_F32 && out_dtype != KVC_DTYPE_BF16))

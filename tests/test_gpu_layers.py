@@ -98,3 +98,41 @@ def test_sixty_four_layers(kvc, oracle_mod):
     assert err == 0
     for l in (0, 17, 63):
         assert_parity(oracle_mod, cases[l], kvs[l], ys[l])
+
+
+@pytest.mark.parametrize("f32,row_pad,block_pad,table", [(True, 0, 0, "col"), (False, 64, 256, "pad"),
+                                                         (True, 32, 8, "row")])
+def test_strided_layers_match_the_oracle(kvc, oracle_mod, f32, row_pad, block_pad, table):
+    # kvc_compress_layers_strided: every layer's state in the same strided
+    # layout (NaN between the rows), one strided block table
+    from test_gpu_strided import Layout
+
+    case = inputs.make_case(2, 4096, 48, seed=inputs.BASE_SEED + 1200 + row_pad, block_size=16,
+                            boundaries_per_req=40, kv_fill=71)
+    L = 3
+    lays = []
+    for l in range(L):
+        st = inputs.fp32_state(case.num_state_blocks, 16, 72 + l) if f32 else \
+            inputs.make_case(2, 4096, 48, seed=inputs.BASE_SEED + 1300 + l, block_size=16,
+                             boundaries_per_req=40).state_bits
+        lays.append(Layout(case, st, row_pad, block_pad, table))
+    devs = [lay.device() for lay in lays]
+    states = [dv[0] for dv in devs]
+    tab = devs[0][1]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    weights = [t(case.rms_norm_weight * (1.0 + 0.1 * l)).float() for l in range(L)]
+    kvs = [t(case.kv_cache) for _ in range(L)]
+    N = case.num_outputs
+    y = torch.zeros((L * N, 512), dtype=torch.float32, device="cuda")
+    kvc.compress_layers(states, t(case.token_to_req), t(case.positions),
+                        t(case.boundary_token_indices), tab, weights, t(case.cos_sin_cache),
+                        t(case.kv_slot_mapping), kvs, 16, 48, y_out=y)
+    assert kvc.kvc_get_device_error(torch.cuda.current_stream().cuda_stream) == 0
+    for l in range(L):
+        lc = inputs.make_case(2, 4096, 48, seed=inputs.BASE_SEED + 1200 + row_pad, block_size=16,
+                              boundaries_per_req=40, kv_fill=71)
+        lc.rms_norm_weight = weights[l].cpu().numpy()
+        ref = lays[l].oracle(oracle_mod, lc)
+        assert ref[1]["status"] == 0
+        assert_parity(oracle_mod, lc, kvs[l].cpu().numpy(), y[l * N:(l + 1) * N].cpu().numpy(),
+                      ref=ref)
