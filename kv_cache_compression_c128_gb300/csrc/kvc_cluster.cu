@@ -416,6 +416,48 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
   }
 }
 
+// Before the grid dependency wait, the previous grid on the stream may still
+// be writing this call's inputs, so nothing read then may reach a result;
+// it may still warm L2.  Lane i resolves unit i of the CTA from the index
+// arrays as they stand (L2-only loads, every index bounds-checked, nothing
+// recorded), which brings the index lines of the resolver's first FIFO
+// block into L2, and the lanes of the first stages prefetch their chunk's
+// rows into L2.  A prefetch changes only what the cache holds and L2 stays
+// coherent with the previous grid's writes, so no result can go stale.  When
+// that grid is still running, this grid's first reads start in its tail
+// instead of after the wait; when none is, they still start before the
+// resolver-to-issuer hand-off.
+template <bool F32>
+__device__ void prefetch_first_stages(const Params& p, int64_t n0, int64_t units, int k_lo, int kj) {
+  using T = StateTraits<F32>;
+  const int lane = threadIdx.x & 31;
+  if (lane >= units) return;
+  const int64_t q = lane / kj;
+  const int kk = lane - static_cast<int>(q) * kj;
+  const int64_t o = n0 + q;
+  const int layer = static_cast<int>(o / p.num_outputs);
+  ChunkRuns cr;
+  MetaRec rec;
+  resolve_chunk_t<true>(p, o - static_cast<int64_t>(layer) * p.num_outputs, k_lo + kk, false, cr, rec);
+  // How much to prefetch, as measured: the first two of the three stages.
+  // The whole first pass made calls with no earlier grid to overlap 1.5-2 us
+  // slower (its prefetches queue ahead of the real copies), and one stage
+  // gains less.  Rows apart take one prefetch per row: the first stage alone.
+  const int first = (p.rows_contiguous ? kStages - 1 : 1) * T::kChunksPerStage;
+  if (cr.off1 < 0 || lane >= first) return;
+  const uint8_t* state = p.states[layer];
+  if (p.rows_contiguous) {
+    bulk_prefetch_l2(state + cr.off1, cr.n1 * T::kRowBytes);
+    if (cr.n2 > 0) bulk_prefetch_l2(state + cr.off2, cr.n2 * T::kRowBytes);
+  } else {
+    for (int r = 0; r < cr.n1 + cr.n2; ++r) {
+      const long long off = r < cr.n1 ? cr.off1 + r * p.state_row_bytes
+                                      : cr.off2 + (r - cr.n1) * p.state_row_bytes;
+      bulk_prefetch_l2(state + off, T::kRowBytes);
+    }
+  }
+}
+
 template <int S, bool F32>
 __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -441,15 +483,18 @@ __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const P
     sh.abort_flag = 0;
     fence_mbar_init();
   }
-  // Wait for the previous grid on the stream (programmatic dependent launch)
-  // before touching any global memory, and let the next one start launching.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (S > 1) {
     cluster_sync_all();  // every rank's barriers exist before any remote store
   } else {
     __syncthreads();
   }
+  // Warp 0 (a consumer warp, idle until the first chunk lands) warms L2; the
+  // other warps go straight on.
+  if (threadIdx.x < 32 && n0 < n1 && kj > 0) prefetch_first_stages<F32>(p, n0, (n1 - n0) * kj, k_lo, kj);
+  // Wait for the previous grid on the stream (programmatic dependent launch)
+  // before reading any input for a result, and let the next one start launching.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (n0 < n1 && kj > 0) {
     const int warp = threadIdx.x >> 5;
     const int64_t units = (n1 - n0) * kj;

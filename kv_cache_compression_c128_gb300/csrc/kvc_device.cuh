@@ -124,6 +124,12 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   return pol;
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16) into L2 from a 16-byte aligned
+// global address.  It moves no data into the SM and completes on nothing.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // One bulk (1-D) copy global -> shared, completing on `bar` as tx bytes.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
                                               unsigned long long* bar, uint64_t policy) {
@@ -361,41 +367,72 @@ struct ChunkRuns {
   int n1, n2;            // rows in each run (n2 = 0: one run)
 };
 
+// Index loads of resolve_chunk_t.  The speculative pass (kSpec) loads
+// through L2 only (ld.global.cg), so it leaves no line in L1 that a load
+// after the grid dependency wait could hit.
+template <bool kSpec>
+__device__ __forceinline__ int64_t ld_index(const int32_t* a) {
+  if constexpr (kSpec) {
+    int32_t v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(a));
+    return v;
+  } else {
+    return __ldg(a);
+  }
+}
+template <bool kSpec>
+__device__ __forceinline__ int64_t ld_index(const int64_t* a) {
+  if constexpr (kSpec) {
+    int64_t v;
+    asm volatile("ld.global.cg.s64 %0, [%1];" : "=l"(v) : "l"(a));
+    return v;
+  } else {
+    return __ldg(a);
+  }
+}
+
 // Resolve chunk k of output n for the cluster route (any window start, any
 // C >= 1, any B >= 8, any state and block-table strides), and, when
 // want_meta, the output's slot and compressed position.  All loads of one
 // level are issued together: the chain before the first copy is boundary
 // index -> (request, position, slot) -> one or two block-table entries.
-__device__ __forceinline__ void resolve_chunk(const Params& p, int64_t n, int k, bool want_meta,
-                                              ChunkRuns& cr, MetaRec& rec) {
+// kSpec: the speculative pass, which runs before the grid dependency wait on
+// indices that may still be changing; every index is bounds-checked all the
+// same (a bad one yields off1 < 0), but nothing is recorded.
+template <bool kSpec>
+__device__ __forceinline__ void resolve_chunk_t(const Params& p, int64_t n, int k, bool want_meta,
+                                                ChunkRuns& cr, MetaRec& rec) {
   cr = ChunkRuns{-1, -1, 0, 0};
   rec = MetaRec{-1, -1};
-  const int64_t b = __ldg(p.bti + n);
-  if (b < 0 || b >= p.num_tokens) { record_error(p.error, kErrBadIndex); return; }
-  const int64_t r = __ldg(p.token_to_req + b);
-  const int64_t pos = __ldg(p.positions + b);
-  const int64_t slot = want_meta ? __ldg(p.slot_map + (p.slot_by_token ? b : n)) : -1;
+  const auto bad = [&]() {
+    if constexpr (!kSpec) record_error(p.error, kErrBadIndex);
+  };
+  const int64_t b = ld_index<kSpec>(p.bti + n);
+  if (b < 0 || b >= p.num_tokens) { bad(); return; }
+  const int64_t r = ld_index<kSpec>(p.token_to_req + b);
+  const int64_t pos = ld_index<kSpec>(p.positions + b);
+  const int64_t slot = want_meta ? ld_index<kSpec>(p.slot_map + (p.slot_by_token ? b : n)) : -1;
   const int64_t C = p.compress_ratio, B = p.block_size;
   const int64_t t0 = pos - C + 1;
-  if (r < 0 || r >= p.num_reqs || t0 < 0) { record_error(p.error, kErrBadIndex); return; }
+  if (r < 0 || r >= p.num_reqs || t0 < 0) { bad(); return; }
   const int64_t first = t0 + static_cast<int64_t>(kBlockRows) * k;
   const int64_t left = C - static_cast<int64_t>(kBlockRows) * k;
   const int nr = static_cast<int>(left < kBlockRows ? left : kBlockRows);
   const int64_t l1 = first / B, o1 = first - l1 * B;
   const int n1 = static_cast<int>(B - o1 < nr ? B - o1 : nr);
   const int n2 = nr - n1;
-  if (l1 + (n2 > 0 ? 1 : 0) >= p.max_blocks) { record_error(p.error, kErrBadIndex); return; }
+  if (l1 + (n2 > 0 ? 1 : 0) >= p.max_blocks) { bad(); return; }
   const int32_t* row = p.block_table + r * p.bt_row_stride;
-  const int64_t g1 = __ldg(row + l1 * p.bt_col_stride);
-  const int64_t g2 = n2 > 0 ? __ldg(row + (l1 + 1) * p.bt_col_stride) : 0;
+  const int64_t g1 = ld_index<kSpec>(row + l1 * p.bt_col_stride);
+  const int64_t g2 = n2 > 0 ? ld_index<kSpec>(row + (l1 + 1) * p.bt_col_stride) : 0;
   if (g1 < 0 || g1 >= p.num_blocks || g2 < 0 || g2 >= p.num_blocks) {
-    record_error(p.error, kErrBadIndex);
+    bad();
     return;
   }
   if (want_meta) {
     const int64_t pc = (pos / C) * C;
     if (pc >= p.num_positions || (slot >= 0 && (slot / kSlotsPerPage) >= p.num_pages)) {
-      record_error(p.error, kErrBadIndex);
+      bad();
       return;
     }
     rec.slot = slot;
@@ -405,6 +442,11 @@ __device__ __forceinline__ void resolve_chunk(const Params& p, int64_t n, int k,
   cr.n1 = n1;
   cr.off2 = n2 > 0 ? g2 * p.state_block_bytes : -1;
   cr.n2 = n2;
+}
+
+__device__ __forceinline__ void resolve_chunk(const Params& p, int64_t n, int k, bool want_meta,
+                                              ChunkRuns& cr, MetaRec& rec) {
+  resolve_chunk_t<false>(p, n, k, want_meta, cr, rec);
 }
 
 // fold_block for a chunk holding only its first `nrows` (1..7) rows: the
