@@ -530,7 +530,7 @@ def bytes_for(case, n_outputs=None, elem_bytes: int = 2) -> int:
 LAYOUTS = {
     "bf16": (2, "contiguous bf16"),
     "fp32_contiguous": (4, "fp32 elements (the seeded bf16 values widened), contiguous"),
-    "bf16_rows_64_apart": (2, "bf16 rows 1088 elements apart: one bulk copy per row"),
+    "bf16_rows_64_apart": (2, "bf16 rows 1088 elements apart: one TMA tensor copy per 8-row chunk"),
     "bf16_blocks_512_apart_colmajor_table": (
         2, "bf16 blocks 8*1024+512 elements apart, column-major block table"),
 }
@@ -781,7 +781,8 @@ def main():
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": traffic,
-                     "kernel": (f"kvc_cluster_kernel<{cluster}, {'true' if f32 else 'false'}>"
+                     "kernel": (f"kvc_cluster_kernel<{cluster}, {'true' if f32 else 'false'}, "
+                                f"{'true' if args.state_layout == 'bf16_rows_64_apart' else 'false'}>"
                                 if cluster else "kvc_streamk_kernel"),
                      "algorithmic_bytes_per_launch": per_call_bytes},
         "gpu_launches": args.steps,

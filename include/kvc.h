@@ -57,15 +57,19 @@ typedef enum {
  *   bits 0..15   force the launch size: clusters for the cluster route, CTAs
  *                for the stream-K route (capped at what fits on the device);
  *   bits 16..20  force the cluster size S (1, 2, 4, 8 or 16, at most C/8);
- *   bit 24       use the stream-K route instead of the cluster route.
- * The routes compute the same bytes (see kvc_query_launch); the flags exist
- * for tuning and testing.  Other bits must be zero.
+ *   bit 24       use the stream-K route instead of the cluster route;
+ *   bit 25       rows apart (kvc_compress_strided): copy one row at a time
+ *                even where a TMA tensor map could move 8 rows at once.
+ * The routes and copy modes compute the same bytes (see kvc_query_launch);
+ * the flags exist for tuning and testing.  Other bits must be zero.
  */
 #define KVC_FLAG_GRID_MASK 0xFFFFu
 #define KVC_FLAG_CLUSTER_SHIFT 16
 #define KVC_FLAG_CLUSTER_MASK (0x1Fu << KVC_FLAG_CLUSTER_SHIFT)
 #define KVC_FLAG_STREAM_K (1u << 24)
-#define KVC_FLAG_ALL (KVC_FLAG_GRID_MASK | KVC_FLAG_CLUSTER_MASK | KVC_FLAG_STREAM_K)
+#define KVC_FLAG_ROW_COPIES (1u << 25)
+#define KVC_FLAG_ALL \
+  (KVC_FLAG_GRID_MASK | KVC_FLAG_CLUSTER_MASK | KVC_FLAG_STREAM_K | KVC_FLAG_ROW_COPIES)
 
 /* Element types: of the state (kvc_compress_strided, kvc_query_launch_ex)
  * and of the output of kvc_dequantize. */
@@ -180,7 +184,12 @@ kvc_status kvc_compress_layers(
  *                     >= 0, in elements; each a multiple of 16 bytes
  *                     (KVC_ERR_UNSUPPORTED otherwise: the rows are moved by
  *                     bulk copies).  Rows that are adjacent (row stride 1024)
- *                     are copied a run at a time, others one row at a time.
+ *                     are copied a run at a time.  Rows apart are copied 8 at
+ *                     a time through a TMA tensor map per layer (calls of up
+ *                     to 8 layers; the library encodes the maps on the host at
+ *                     each call), one at a time where a chunk's 8 rows span
+ *                     two blocks, with more layers, or with
+ *                     KVC_FLAG_ROW_COPIES.
  * block_table         int32; entry (r, l) of request r < num_reqs, logical
  *                     block l < max_blocks_per_req at element offset
  *                     r * block_table_row_stride + l * block_table_col_stride

@@ -40,16 +40,21 @@ KVC_DTYPE_F32 = 0
 KVC_DTYPE_BF16 = 1
 KVC_FLAG_CLUSTER_SHIFT = 16
 KVC_FLAG_STREAM_K = 1 << 24
+KVC_FLAG_ROW_COPIES = 1 << 25
 
 
-def make_flags(route: str = "auto", count: int = 0, cluster_size: int = 0) -> int:
+def make_flags(route: str = "auto", count: int = 0, cluster_size: int = 0,
+               row_copies: bool = False) -> int:
     """kvc_compress flags: route 'auto' | 'cluster' | 'streamk', a forced
-    launch size (clusters or CTAs; 0 = automatic) and cluster size."""
+    launch size (clusters or CTAs; 0 = automatic), cluster size, and, for
+    rows apart, row-by-row copies instead of TMA tensor maps."""
     f = int(count) & KVC_FLAG_GRID_MASK
     if route == "streamk":
         f |= KVC_FLAG_STREAM_K
     else:
         f |= (int(cluster_size) & 0x1F) << KVC_FLAG_CLUSTER_SHIFT
+    if row_copies:
+        f |= KVC_FLAG_ROW_COPIES
     return f
 
 HEAD_DIM = 512

@@ -19,6 +19,7 @@ namespace {
 __device__ uint32_t g_error_word;
 
 constexpr int kMaxDevices = 64;
+
 constexpr int kClusterSizes[] = {1, 2, 4, 8, 16};
 constexpr int kNumClusterSizes = 5;
 
@@ -310,6 +311,14 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, const Sta
   if (!pick_route(d, num_outputs * L, p.blocks_per_output, streamk_ok, chunk, flags, &r))
     return KVC_ERR_UNSUPPORTED;
   p.cluster_size = r.cluster;
+  if (!r.stream_k && !p.rows_contiguous && L <= kvc::kMaxMapLayers &&
+      (flags & KVC_FLAG_ROW_COPIES) == 0) {
+    bool ok = true;
+    for (int l = 0; l < L && ok; ++l)
+      ok = kvc::encode_rows_map(&p.maps[l], state_caches[l], p.state_f32 != 0, block_size,
+                           num_state_blocks, p.state_row_bytes, p.state_block_bytes);
+    p.use_maps = ok ? 1 : 0;
+  }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!r.stream_k) return kvc::launch_cluster(p, r.count, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
   // stream-K: one launch per layer (each reuses the workspace, in stream order)

@@ -80,7 +80,7 @@ struct alignas(16) FifoEntry {
   int kk;                // chunk index within this CTA's range of its output
   int piece;             // output index relative to the cluster's first output
   int layer;             // layer whose state cache the chunk is read from
-  int pad_;
+  int g1, o1;            // block and first row of run 1 (for a tensor copy)
 };
 
 template <int S>
@@ -109,13 +109,15 @@ __device__ __forceinline__ bool aborted(const int* flag) {
 
 __device__ __forceinline__ void set_abort(int* flag) { *reinterpret_cast<volatile int*>(flag) = 1; }
 
-template <int S>
+// kBlocks: also pass each chunk's block and first row (tensor copies need
+// them; adjacent rows leave the two fields alone).
+template <int S, bool kBlocks>
 __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int64_t units, int k_lo,
                          int kj) {
   const int lane = threadIdx.x & 31;
   for (int64_t c = 0; c * kFifoChunk < units; ++c) {
     const int64_t i = c * kFifoChunk + lane;
-    FifoEntry e{-1, -1, -1, -1, 0, 0, 0, 0, 0, 0};
+    FifoEntry e{-1, -1, -1, -1, 0, 0, 0, 0, 0, 0, 0};
     if (i < units) {
       const int64_t q = i / kj;
       const int kk = static_cast<int>(i - q * kj);
@@ -129,6 +131,10 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int6
       e.off2 = cr.off2;
       e.n1 = cr.n1;
       e.n2 = cr.n2;
+      if (kBlocks) {
+        e.g1 = cr.g1;
+        e.o1 = cr.o1;
+      }
       e.slot = rec.slot;
       e.pc = rec.pc;
       e.kk = kk;
@@ -152,16 +158,27 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int6
   }
 }
 
-// kSplitRows = false: rows of a block are adjacent; lane 0 alone walks the
-// FIFO and issues one copy per run of rows (the other lanes leave at once).
-// kSplitRows = true: rows are apart; the whole warp walks the FIFO (lane 0
-// waits, announces bytes and arrives) and the copies of a chunk are issued
-// one row per lane, so their issue does not serialise on one thread (measured
-// 67.2 -> 53.8 us at the headline with rows 64 elements apart, while the
-// warp-wide walk costs the adjacent-row case up to 1.5 %).
-template <int S, bool F32, bool kSplitRows>
+// How the issuer moves a chunk's rows into the ring.
+//   kRuns:   rows of a block are adjacent; one bulk copy per run of rows.
+//   kTensor: rows are apart and the layer has a TMA tensor map; one tensor
+//            copy moves a chunk whose 8 rows lie in one block (a 256 x 4 x 8
+//            box), and a chunk split between two blocks goes row by row.
+//   kRows:   rows are apart, no map; one bulk copy per row, issued by the
+//            lanes of the warp in parallel.
+// Each copy has a fixed cost in the TMA unit, so eight 2 KiB copies take far
+// longer than one of 16 KiB: with rows 64 elements apart the headline took
+// 67.2 us with one lane issuing row copies, 52.0 us with eight lanes (kRows)
+// and 42 us with tensor copies; per-row copies on adjacent rows were as slow
+// (52.9 us), so the layout itself costs nothing.
+enum class Copy { kRuns, kTensor, kRows };
+
+// kRuns, kTensor: lane 0 alone walks the FIFO (the other lanes leave at
+// once).  kRows: the whole warp walks it (lane 0 waits, announces bytes and
+// arrives; the walk costs about 2.5 % against lane 0 alone).
+template <int S, bool F32, Copy kCopy>
 __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int64_t units, int kj) {
   using T = StateTraits<F32>;
+  constexpr bool kSplitRows = kCopy == Copy::kRows;
   const int lane = threadIdx.x & 31;
   if (!kSplitRows && lane != 0) return;
   const auto lane0_says = [](bool v) { return kSplitRows ? __shfl_sync(0xffffffffu, v, 0) : v; };
@@ -225,11 +242,21 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
           }
         }
         const uint8_t* state = p.states[e.layer];
-        if constexpr (!kSplitRows) {
+        if constexpr (kCopy == Copy::kRuns) {
           bulk_copy_g2s(dst, state + e.off1, e.n1 * kRowBytes, &sh.full_bar[stage], policy);
           if (e.n2 > 0)
             bulk_copy_g2s(dst + e.n1 * kRowBytes, state + e.off2, e.n2 * kRowBytes,
                           &sh.full_bar[stage], policy);
+        } else if constexpr (kCopy == Copy::kTensor) {
+          if (e.n1 == kBlockRows) {
+            tensor_copy_g2s(dst, &p.maps[e.layer], e.o1, e.g1, &sh.full_bar[stage], policy);
+          } else {
+            for (int r = 0; r < nr; ++r) {
+              const long long off = r < e.n1 ? e.off1 + r * p.state_row_bytes
+                                             : e.off2 + (r - e.n1) * p.state_row_bytes;
+              bulk_copy_g2s(dst + r * kRowBytes, state + off, kRowBytes, &sh.full_bar[stage], policy);
+            }
+          }
         } else {
           __syncwarp();  // the bytes are announced before any row copy is issued
           if (lane < nr) {
@@ -428,7 +455,8 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
 // instead of after the wait; when none is, they still start before the
 // resolver-to-issuer hand-off.
 template <bool F32>
-__device__ void prefetch_first_stages(const Params& p, int64_t n0, int64_t units, int k_lo, int kj) {
+__device__ void prefetch_first_stages(const Params& p, int64_t n0, int64_t units, int k_lo, int kj,
+                                      bool maps) {
   using T = StateTraits<F32>;
   const int lane = threadIdx.x & 31;
   if (lane >= units) return;
@@ -442,13 +470,16 @@ __device__ void prefetch_first_stages(const Params& p, int64_t n0, int64_t units
   // How much to prefetch, as measured: the first two of the three stages.
   // The whole first pass made calls with no earlier grid to overlap 1.5-2 us
   // slower (its prefetches queue ahead of the real copies), and one stage
-  // gains less.  Rows apart take one prefetch per row: the first stage alone.
-  const int first = (p.rows_contiguous ? kStages - 1 : 1) * T::kChunksPerStage;
+  // gains less.  Rows apart without a map take one prefetch per row: the
+  // first stage alone.
+  const int first = (p.rows_contiguous || maps ? kStages - 1 : 1) * T::kChunksPerStage;
   if (cr.off1 < 0 || lane >= first) return;
   const uint8_t* state = p.states[layer];
   if (p.rows_contiguous) {
     bulk_prefetch_l2(state + cr.off1, cr.n1 * T::kRowBytes);
     if (cr.n2 > 0) bulk_prefetch_l2(state + cr.off2, cr.n2 * T::kRowBytes);
+  } else if (maps && cr.n1 == kBlockRows) {
+    tensor_prefetch_l2(&p.maps[layer], cr.o1, cr.g1);
   } else {
     for (int r = 0; r < cr.n1 + cr.n2; ++r) {
       const long long off = r < cr.n1 ? cr.off1 + r * p.state_row_bytes
@@ -458,8 +489,14 @@ __device__ void prefetch_first_stages(const Params& p, int64_t n0, int64_t units
   }
 }
 
-template <int S, bool F32>
-__global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const Params p) {
+// kApart: the rows of a block are apart (tensor or row copies); otherwise
+// adjacent (run copies).  The tensor-copy path lives in the kApart kernels
+// only: in the same kernel as the run copies it cost the adjacent-row
+// headline 0.4-0.6 %.  The parameters are __grid_constant__ so that the
+// tensor maps in them can be addressed in place by the TMA unit.
+template <int S, bool F32, bool kApart>
+__global__ void __launch_bounds__(kClusterThreads, 2)
+    kvc_cluster_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   ClusterShared<S>& sh = *reinterpret_cast<ClusterShared<S>*>(smem + kRingBytes);
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
@@ -488,9 +525,14 @@ __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const P
   } else {
     __syncthreads();
   }
+  // Tensor copies need the ring 128-byte aligned and the maps 64-byte aligned;
+  // failing either, rows apart go row by row.
+  const bool maps = kApart && p.use_maps && (smem_addr(smem) & 127u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(&p.maps[0]) & 63u) == 0;
   // Warp 0 (a consumer warp, idle until the first chunk lands) warms L2; the
   // other warps go straight on.
-  if (threadIdx.x < 32 && n0 < n1 && kj > 0) prefetch_first_stages<F32>(p, n0, (n1 - n0) * kj, k_lo, kj);
+  if (threadIdx.x < 32 && n0 < n1 && kj > 0)
+    prefetch_first_stages<F32>(p, n0, (n1 - n0) * kj, k_lo, kj, maps);
   // Wait for the previous grid on the stream (programmatic dependent launch)
   // before reading any input for a result, and let the next one start launching.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -499,12 +541,18 @@ __global__ void __launch_bounds__(kClusterThreads, 2) kvc_cluster_kernel(const P
     const int warp = threadIdx.x >> 5;
     const int64_t units = (n1 - n0) * kj;
     if (warp == kResolverWarp) {
-      resolver<S>(p, sh, n0, units, k_lo, kj);
+      resolver<S, kApart>(p, sh, n0, units, k_lo, kj);
     } else if (warp == kIssuerWarp) {
-      if (p.rows_contiguous) {
-        issuer<S, F32, false>(p, sh, smem, units, kj);
+      if constexpr (!kApart) {
+        // Rows are adjacent whenever this kernel runs.  The row-copy branch
+        // stays in its code all the same: without it the kernel's code layout
+        // changed and the 64 MiB C = 128 shape measured 1.5 % slower.
+        if (p.rows_contiguous) issuer<S, F32, Copy::kRuns>(p, sh, smem, units, kj);
+        else issuer<S, F32, Copy::kRows>(p, sh, smem, units, kj);
+      } else if (maps) {
+        issuer<S, F32, Copy::kTensor>(p, sh, smem, units, kj);
       } else {
-        issuer<S, F32, true>(p, sh, smem, units, kj);
+        issuer<S, F32, Copy::kRows>(p, sh, smem, units, kj);
       }
     } else {
       consumers<S, F32>(p, sh, smem, n0, n1, kj, rank);
@@ -536,9 +584,9 @@ cudaLaunchConfig_t config_of(int clusters, cudaStream_t stream, cudaLaunchAttrib
   return cfg;
 }
 
-template <int S, bool F32>
+template <int S, bool F32, bool kApart>
 int prepare_and_capacity() {
-  const void* fn = reinterpret_cast<const void*>(&kvc_cluster_kernel<S, F32>);
+  const void* fn = reinterpret_cast<const void*>(&kvc_cluster_kernel<S, F32, kApart>);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes_of<S>())) != cudaSuccess)
     return 0;
@@ -548,30 +596,93 @@ int prepare_and_capacity() {
   cudaLaunchConfig_t cfg = config_of<S>(1, nullptr, attrs);
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, &kvc_cluster_kernel<S, F32>, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, &kvc_cluster_kernel<S, F32, kApart>, &cfg) != cudaSuccess)
+    return 0;
   return n;
 }
 
-// Both element types share the footprint; the capacity is the smaller one.
+// Every kernel of a cluster size shares the footprint; the capacity is the
+// smallest one.
 template <int S>
 int prepare_and_capacity_both() {
-  const int a = prepare_and_capacity<S, false>();
-  const int b = prepare_and_capacity<S, true>();
-  return a < b ? a : b;
+  const int c[4] = {prepare_and_capacity<S, false, false>(), prepare_and_capacity<S, true, false>(),
+                    prepare_and_capacity<S, false, true>(), prepare_and_capacity<S, true, true>()};
+  int n = c[0];
+  for (int i = 1; i < 4; ++i) n = c[i] < n ? c[i] : n;
+  return n;
 }
 
 template <int S>
 cudaError_t launch_of(const Params& p, int clusters, cudaStream_t stream) {
   cudaLaunchAttribute attrs[2];
   cudaLaunchConfig_t cfg = config_of<S>(clusters, stream, attrs);
-  const cudaError_t e = p.state_f32 ? cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S, true>, p)
-                                    : cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S, false>, p);
+  cudaError_t e;
+  if (p.rows_contiguous) {
+    e = p.state_f32 ? cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S, true, false>, p)
+                    : cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S, false, false>, p);
+  } else {
+    e = p.state_f32 ? cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S, true, true>, p)
+                    : cudaLaunchKernelEx(&cfg, &kvc_cluster_kernel<S, false, true>, p);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
 
 int cluster_threads() { return kClusterThreads; }
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against
+// the driver library).  Null when the driver does not offer it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+namespace {
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      (void)cudaGetLastError();
+      return static_cast<EncodeTiledFn>(nullptr);
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+// The TMA tensor map of one layer's state when its rows are apart: the 4-D
+// view (256 elements, 4 row segments, block_size rows, num_blocks blocks)
+// with strides (256 elements, row stride, block stride) in bytes, and a box
+// of 8 whole rows.  L2 fills in 128-byte granules: rows start on 128-byte
+// boundaries, and 256-byte fills read 3 % more than the rows (part of the
+// gap after every other row).  False when the driver refuses the map or a
+// coordinate would not fit the 32-bit tensor coordinates; the call then
+// copies row by row.
+bool encode_rows_map(CUtensorMap* m, const void* base, bool f32, int64_t block_size,
+                     int64_t num_blocks, int64_t row_bytes, int64_t block_bytes) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn || num_blocks > INT32_MAX || block_size > INT32_MAX || row_bytes <= 0 ||
+      block_bytes <= 0 || row_bytes >= (int64_t{1} << 40) || block_bytes >= (int64_t{1} << 40))
+    return false;
+  const cuuint64_t esize = f32 ? 4 : 2;
+  const cuuint64_t dims[4] = {kMapInner, kMapSegments, static_cast<cuuint64_t>(block_size),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {kMapInner * esize, static_cast<cuuint64_t>(row_bytes),
+                                 static_cast<cuuint64_t>(block_bytes)};
+  const cuuint32_t box[4] = {kMapInner, kMapSegments, kBlockRows, 1};
+  const cuuint32_t unit[4] = {1, 1, 1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+            const_cast<void*>(base), dims, strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 size_t cluster_smem_bytes(int S) {
   switch (S) {

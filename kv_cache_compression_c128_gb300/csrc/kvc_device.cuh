@@ -124,6 +124,26 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   return pol;
 }
 
+// One tensor copy global -> shared through the 4-D map `map` (a generic
+// address of a CUtensorMap in parameter space): the box at element
+// coordinates (0, 0, row, block), completing on `bar` as tx bytes.  `dst`
+// 128-byte aligned.
+__device__ __forceinline__ void tensor_copy_g2s(void* dst, const void* map, int row, int block,
+                                                unsigned long long* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(0), "r"(0), "r"(row), "r"(block), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// The same box prefetched into L2.
+__device__ __forceinline__ void tensor_prefetch_l2(const void* map, int row, int block) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map),
+               "r"(0), "r"(0), "r"(row), "r"(block)
+               : "memory");
+}
+
 // Bulk prefetch of `bytes` (a multiple of 16) into L2 from a 16-byte aligned
 // global address.  It moves no data into the SM and completes on nothing.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
@@ -365,6 +385,7 @@ __device__ __forceinline__ void resolve_unit(const Params& p, int64_t n, int k, 
 struct ChunkRuns {
   long long off1, off2;  // byte offset of each run's first row (off1 < 0: bad chunk)
   int n1, n2;            // rows in each run (n2 = 0: one run)
+  int g1, o1;            // block and first row of run 1 (g1 valid below 2^31 only)
 };
 
 // Index loads of resolve_chunk_t.  The speculative pass (kSpec) loads
@@ -402,7 +423,7 @@ __device__ __forceinline__ int64_t ld_index(const int64_t* a) {
 template <bool kSpec>
 __device__ __forceinline__ void resolve_chunk_t(const Params& p, int64_t n, int k, bool want_meta,
                                                 ChunkRuns& cr, MetaRec& rec) {
-  cr = ChunkRuns{-1, -1, 0, 0};
+  cr = ChunkRuns{-1, -1, 0, 0, 0, 0};
   rec = MetaRec{-1, -1};
   const auto bad = [&]() {
     if constexpr (!kSpec) record_error(p.error, kErrBadIndex);
@@ -442,6 +463,8 @@ __device__ __forceinline__ void resolve_chunk_t(const Params& p, int64_t n, int 
   cr.n1 = n1;
   cr.off2 = n2 > 0 ? g2 * p.state_block_bytes : -1;
   cr.n2 = n2;
+  cr.g1 = static_cast<int>(g1);
+  cr.o1 = static_cast<int>(o1);
 }
 
 __device__ __forceinline__ void resolve_chunk(const Params& p, int64_t n, int k, bool want_meta,

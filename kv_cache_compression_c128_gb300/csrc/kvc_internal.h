@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>  // CUtensorMap (a plain struct; no driver call is linked)
 #include <cuda_runtime.h>
 
 namespace kvc {
@@ -43,6 +44,17 @@ constexpr int kPartialFloats = 3 * kHeadDim;
 // kernel parameters).
 constexpr int kMaxLayers = 64;
 
+// Layers that get a TMA tensor map when the rows of a block are apart (one
+// tensor copy per full 8-row run instead of one bulk copy per row).  The maps
+// travel in the kernel parameters, 128 bytes each.
+constexpr int kMaxMapLayers = 8;
+
+// The 4-D view of a state that the maps describe, innermost first: 256
+// elements, 4 segments of a row (kRowElems = 4 x 256), rows of a block,
+// blocks; the box is 256 x 4 x 8 x 1, i.e. 8 whole rows.
+constexpr int kMapInner = 256;
+constexpr int kMapSegments = kRowElems / kMapInner;
+
 struct Params {
   const uint8_t* states[kMaxLayers];   // per layer: state base (bf16 or fp32 elements)
   const float* weights[kMaxLayers];    // per layer: rms_norm_weight [512]
@@ -79,6 +91,8 @@ struct Params {
   int32_t* part_status;           // [2 * max_ctas]
   int32_t* counters;              // [num_outputs]
   uint32_t* error;                // device error word (first error code wins)
+  int use_maps;                   // rows apart and every layer has a map (cluster route)
+  CUtensorMap maps[kMaxMapLayers];  // per layer, when use_maps
 };
 
 // Workspace layout (byte offsets), given the device's CTA capacity.
@@ -98,6 +112,10 @@ int cluster_threads();
 size_t cluster_smem_bytes(int cluster_size);
 int cluster_capacity(int cluster_size);  // sets the kernel up; co-resident clusters (0: refused)
 cudaError_t launch_cluster(const Params& p, int clusters, cudaStream_t stream);
+// The TMA tensor map of one layer's state with rows apart (host; false when
+// it cannot be encoded, and the call then copies row by row).
+bool encode_rows_map(CUtensorMap* map, const void* base, bool f32, int64_t block_size,
+                     int64_t num_blocks, int64_t row_bytes, int64_t block_bytes);
 
 // reader direction (kvc_reader.cu)
 cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_t* slots,

@@ -112,6 +112,26 @@ def test_make_flags(kvc):
     assert kvc.make_flags() == 0
     assert kvc.make_flags("cluster", 3, 8) == 3 | (8 << 16)
     assert kvc.make_flags("streamk", 13) == 13 | (1 << 24)
+    assert kvc.make_flags(row_copies=True) == 1 << 25
+
+
+def test_flag_constants_match_the_header(kvc):
+    # the Python constants and the header's #defines name the same bits
+    import os
+
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "kvc.h")).read()
+    for name, value in (("KVC_FLAG_STREAM_K", kvc.KVC_FLAG_STREAM_K),
+                        ("KVC_FLAG_ROW_COPIES", kvc.KVC_FLAG_ROW_COPIES)):
+        m = re.search(r"#define %s \(1u << (\d+)\)" % name, hdr)
+        assert m and (1 << int(m.group(1))) == value
+
+
+def test_row_copies_flag_is_accepted(kvc):
+    # bit 25 is a known flag: the call gets past the flag check (an unknown
+    # bit returns INVALID_ARG) to the block-size check (UNSUPPORTED)
+    small = dict(_GOOD, block_size=4)
+    assert kvc.kvc_compress(**dict(small, flags=kvc.KVC_FLAG_ROW_COPIES)) == 2
+    assert kvc.kvc_compress(**dict(small, flags=1 << 26)) == 1
 
 
 def test_torch_wrapper_rejects_cpu_tensors(kvc):

@@ -6,7 +6,8 @@ Each seed draws one call at random:
   600, windows at random starts;
 - slots given per token or per output, a few of them -1 (skipped);
 - a bf16 or fp32 state, adjacent or padded rows and blocks, a row-major or
-  column-major block table;
+  column-major block table; rows apart copied through tensor maps or row by
+  row;
 - an automatic or forced cluster size, or the stream-K route where it
   applies.
 
@@ -69,12 +70,13 @@ def _draw(seed):
         routes.append("streamk")
     route = str(rng.choice(routes))
     count = int(rng.choice([0, 0, 1, 3, 17]))
-    return case, slots, f32, row_pad, block_pad, table, route, count
+    row_copies = bool(rng.integers(0, 2)) if row_pad else False
+    return case, slots, f32, row_pad, block_pad, table, route, count, row_copies
 
 
 @pytest.mark.parametrize("seed", range(4000, 4120))
 def test_random_configuration(kvc, oracle_mod, seed):
-    case, slots, f32, row_pad, block_pad, table, route, count = _draw(seed)
+    case, slots, f32, row_pad, block_pad, table, route, count, row_copies = _draw(seed)
     state = inputs.fp32_state(case.num_state_blocks, case.block_size, seed + 1) if f32 \
         else case.state_bits
     G, B, _ = state.shape
@@ -107,6 +109,8 @@ def test_random_configuration(kvc, oracle_mod, seed):
         flags = kvc.make_flags("streamk", count)
     else:
         flags = kvc.make_flags("cluster", count, int(route[1:]))
+    if row_copies:
+        flags |= kvc.KVC_FLAG_ROW_COPIES
     kvc.c128_256_512_compress(st, t(case.token_to_req), t(case.positions),
                               t(case.boundary_token_indices), bt, t(case.rms_norm_weight),
                               t(case.cos_sin_cache), t(slots), kv, B, case.compress_ratio,

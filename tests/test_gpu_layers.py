@@ -100,16 +100,18 @@ def test_sixty_four_layers(kvc, oracle_mod):
         assert_parity(oracle_mod, cases[l], kvs[l], ys[l])
 
 
-@pytest.mark.parametrize("f32,row_pad,block_pad,table", [(True, 0, 0, "col"), (False, 64, 256, "pad"),
-                                                         (True, 32, 8, "row")])
-def test_strided_layers_match_the_oracle(kvc, oracle_mod, f32, row_pad, block_pad, table):
+@pytest.mark.parametrize("f32,row_pad,block_pad,table,L", [
+    (True, 0, 0, "col", 3), (False, 64, 256, "pad", 3), (True, 32, 8, "row", 3),
+    (False, 64, 0, "row", 8),    # rows apart: the most layers that get tensor maps
+    (False, 64, 0, "row", 9),    # one more: every layer goes row by row
+])
+def test_strided_layers_match_the_oracle(kvc, oracle_mod, f32, row_pad, block_pad, table, L):
     # kvc_compress_layers_strided: every layer's state in the same strided
     # layout (NaN between the rows), one strided block table
     from test_gpu_strided import Layout
 
     case = inputs.make_case(2, 4096, 48, seed=inputs.BASE_SEED + 1200 + row_pad, block_size=16,
                             boundaries_per_req=40, kv_fill=71)
-    L = 3
     lays = []
     for l in range(L):
         st = inputs.fp32_state(case.num_state_blocks, 16, 72 + l) if f32 else \

@@ -222,3 +222,36 @@ def test_bf16_split_rows_headline_shape_full_size(kvc, oracle_mod):
     case = inputs.headline_case()
     lay = Layout(case, case.state_bits, row_pad=64, block_pad=0, table="pad")
     check_layout(kvc, oracle_mod, case, lay)
+
+
+# ---- rows apart: tensor-map copies against row-by-row copies ---------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("C,B,nb,route", [
+    (128, 8, None, "auto"),     # aligned windows: every chunk is one tensor copy
+    (256, 8, None, "s4"),       # the same through a cluster of 4
+    (48, 16, 50, "auto"),       # general windows: chunks split between blocks go row by row
+    (100, 24, 40, "s2"),
+    (512, 64, 12, "auto"),
+])
+def test_rows_apart_tensor_and_row_copies_agree(kvc, oracle_mod, dtype, C, B, nb, route):
+    # Rows apart are copied 8 at a time through a TMA tensor map per layer;
+    # with KVC_FLAG_ROW_COPIES one bulk copy per row.  Both fill the ring with
+    # the same bytes, so results are identical, and both meet the bar.  The
+    # gaps between rows hold NaN, so a box that strayed would show.
+    T = 3 * (2064 if B == 24 else 2048)  # requests of whole blocks
+    case = inputs.make_case(3, T, C, seed=inputs.BASE_SEED + 880 + C, block_size=B,
+                            boundaries_per_req=nb, kv_fill=94)
+    f32 = dtype == "f32"
+    st = _fp32(case, 95) if f32 else case.state_bits
+    lay = Layout(case, st, row_pad=32 if f32 else 64, block_pad=256, table="pad")
+    S = 0 if route == "auto" else int(route[1:])
+    flags = kvc.make_flags("auto" if S == 0 else "cluster", 0, S)
+    kv_t, y_t, e_t = run_layout(kvc, case, lay, flags)
+    kv_r, y_r, e_r = run_layout(kvc, case, lay, flags | kvc.KVC_FLAG_ROW_COPIES)
+    assert e_t == 0 and e_r == 0 and case.num_outputs > 0
+    assert np.array_equal(kv_t, kv_r)
+    assert np.array_equal(y_t.view(np.uint32), y_r.view(np.uint32))
+    ref = lay.oracle(oracle_mod, case)
+    assert ref[1]["status"] == 0
+    assert_parity(oracle_mod, case, kv_t, y_t, ref=ref)
