@@ -231,6 +231,85 @@ __global__ void __launch_bounds__(kReaderThreads) kvc_dequant_warp_kernel(
   }
 }
 
+// bf16 output of a large call into 16-byte-aligned memory: lane L covers
+// dims 256k + 8L .. 256k + 8L + 7 of the slot (k = 0, 1), so a slot is one
+// 8-byte code load per lane and half (lanes 24..31 of half 1 load the 16
+// bytes of RoPE words instead), the 8-byte scale record, and one 16-byte
+// store per lane and half: 512-byte store instructions, half as many as the
+// 4-dims-per-lane layout.  Same values, bit for bit.
+template <int kUnroll>
+__global__ void __launch_bounds__(kReaderThreads) kvc_dequant_wide16_kernel(
+    const uint8_t* __restrict__ kv, int64_t num_pages, const int64_t* __restrict__ slots,
+    int64_t num_slots, uint16_t* __restrict__ out, uint32_t* err) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  constexpr int kWarps = kReaderThreads / 32;
+  const int lane = threadIdx.x & 31;
+  const bool rope_lane = lane >= 24;  // in half 1: dims 448..511
+  const int64_t width = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+       base < num_slots; base += width * kUnroll) {
+    int64_t sl[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t m = base + u * width;
+      sl[u] = m < num_slots ? __ldg(slots + m) : -1;
+    }
+    uint2 codes[kUnroll][2], scale[kUnroll];
+    uint4 rope[kUnroll];
+    bool ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      codes[u][0] = codes[u][1] = scale[u] = make_uint2(0u, 0u);
+      rope[u] = make_uint4(0u, 0u, 0u, 0u);
+      ok[u] = false;
+      if (sl[u] < 0) continue;
+      const int64_t page = sl[u] / kSlotsPerPage, off = sl[u] % kSlotsPerPage;
+      if (page >= num_pages) {
+        if (lane == 0) atomicCAS(err, 0u, kErrBadIndexReader);
+        continue;
+      }
+      const uint8_t* pg = kv + page * kPageBytes;
+      const uint8_t* payload = pg + off * kTokenStride;
+      scale[u] = __ldg(reinterpret_cast<const uint2*>(pg + kScaleBase + off * kScaleDim));
+      codes[u][0] = __ldg(reinterpret_cast<const uint2*>(payload + 8 * lane));
+      if (!rope_lane)
+        codes[u][1] = __ldg(reinterpret_cast<const uint2*>(payload + 256 + 8 * lane));
+      else
+        rope[u] = __ldg(reinterpret_cast<const uint4*>(payload + kNopeDim + 16 * (lane - 24)));
+      ok[u] = true;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t m = base + u * width;
+      if (m >= num_slots) continue;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int d = 256 * k + 8 * lane;
+        uint4 o;
+        if (k == 1 && rope_lane) {  // the stored bf16 words, copied as they are
+          o = rope[u];
+        } else {
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+          if (ok[u]) {
+            const int g = d / kGroup;
+            const uint32_t sw = g < 4 ? scale[u].x : scale[u].y;
+            const int e = static_cast<int>((sw >> (8 * (g & 3))) & 0xFFu) - 127;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t word = i < 4 ? codes[u][k].x : codes[u][k].y;
+              const float v = ldexpf(static_cast<float>(static_cast<int8_t>((word >> (8 * (i & 3))) & 0xFFu)), e);
+              w[i / 2] |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << (16 * (i & 1));
+            }
+          }
+          o = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        *reinterpret_cast<uint4*>(out + m * kHeadDim + d) = o;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -242,6 +321,7 @@ namespace {
 //   streaming stores or more slots made it 4-27 % slower).
 #define KVC_WARP_F32 kvc_dequant_warp_kernel<8, true>
 #define KVC_WARP_BF16 kvc_dequant_warp_kernel<2, false>
+#define KVC_WIDE16_BF16 kvc_dequant_wide16_kernel<2>
 
 // CTAs of a kernel that fit on the current device at once (cached per device).
 int resident_ctas(int dev, const void* kernel, std::atomic<int>* cache) {
@@ -263,14 +343,16 @@ int resident_ctas(int dev, const void* kernel, std::atomic<int>* cache) {
 cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_t* slots,
                               int64_t num_slots, void* out, int out_bf16, uint32_t* err,
                               cudaStream_t stream) {
-  static std::atomic<int> small_cap[64], f32_cap[64], bf16_cap[64];  // per device, 0: unknown
+  static std::atomic<int> small_cap[64], f32_cap[64], bf16_cap[64], wide_cap[64];  // 0: unknown
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   const void* small_fn = reinterpret_cast<const void*>(&kvc_dequant_kernel<1>);
-  const void* large_fn = out_bf16 ? reinterpret_cast<const void*>(&KVC_WARP_BF16)
-                                  : reinterpret_cast<const void*>(&KVC_WARP_F32);
+  const bool wide16 = out_bf16 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  const void* large_fn = wide16     ? reinterpret_cast<const void*>(&KVC_WIDE16_BF16)
+                         : out_bf16 ? reinterpret_cast<const void*>(&KVC_WARP_BF16)
+                                    : reinterpret_cast<const void*>(&KVC_WARP_F32);
   const int cap_s = resident_ctas(dev, small_fn, small_cap);
-  const int cap_l = resident_ctas(dev, large_fn, out_bf16 ? bf16_cap : f32_cap);
+  const int cap_l = resident_ctas(dev, large_fn, wide16 ? wide_cap : out_bf16 ? bf16_cap : f32_cap);
   if (cap_s == 0 || cap_l == 0) return cudaErrorInvalidDevice;
   // up to a device-full of slot pairs: one CTA per pair, 128 threads per slot
   // (the shortest chain); beyond that a persistent grid of warp-per-slot CTAs
@@ -290,6 +372,9 @@ cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_
   if (!large) {
     e = cudaLaunchKernelEx(&cfg, &kvc_dequant_kernel<1>, kv, num_pages, slots, num_slots, out,
                            out_bf16, err);
+  } else if (wide16) {
+    e = cudaLaunchKernelEx(&cfg, &KVC_WIDE16_BF16, kv, num_pages, slots, num_slots,
+                           static_cast<uint16_t*>(out), err);
   } else if (out_bf16) {
     e = cudaLaunchKernelEx(&cfg, &KVC_WARP_BF16, kv, num_pages, slots, num_slots, out, out_bf16, err);
   } else {

@@ -106,3 +106,27 @@ def test_reader_large_calls_exact_on_random_bytes(kvc, oracle_mod, M):
     want, st = oracle_mod.dequantize(kv, bad)
     assert e == 4 and st == 4
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [20011, 120000])
+def test_reader_large_bf16_into_8_byte_aligned_output(kvc, oracle_mod, M):
+    # bf16 output needs only 8-byte alignment: a 16-byte-aligned output takes
+    # the 8-dims-per-lane kernel (the test above), an output 8 bytes off a
+    # 16-byte boundary the 4-dims-per-lane one; both must read back the
+    # oracle's bits
+    rng = np.random.default_rng(47 + M)
+    pages = 64
+    kv = rng.integers(0, 256, size=(pages, 37376), dtype=np.uint8)
+    slots = rng.integers(0, pages * 64, size=M).astype(np.int64)
+    slots[rng.choice(M, size=M // 50, replace=False)] = -1
+    buf = torch.full((M * 512 + 4,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[4:].view(M, 512)
+    assert out.data_ptr() % 16 == 8
+    kvc.dequantize(torch.from_numpy(kv).cuda(), torch.from_numpy(slots).cuda(),
+                   dtype=torch.bfloat16, out=out)
+    assert kvc.kvc_get_device_error(torch.cuda.current_stream().cuda_stream) == 0
+    want, st = oracle_mod.dequantize(kv, slots, out_bf16=True)
+    assert st == 0
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, want.view(np.uint16))
+    assert torch.isnan(buf[:4]).all()
