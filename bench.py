@@ -450,7 +450,12 @@ def time_layers(kvc, case, device, L: int = 8, steps: int = 1000):
 
 def time_e2e(kvc, case, device, steps: int, warmup: int):
     """Seconds per call through the public API from pinned host buffers:
-    H2D of every input, the call, D2H of kv_cache, all inside the region."""
+    every step copies all of its inputs host->device, makes the call, and
+    reads kv_cache back device->host, all inside the timed region.  Two
+    device input sets alternate, so one step's copy-in runs on a copy
+    stream while the previous step computes and copies out on the compute
+    stream (each step waits for its own inputs; a buffer is refilled only
+    after the step that used it has copied its result out)."""
     import torch
 
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -460,35 +465,49 @@ def time_e2e(kvc, case, device, steps: int, warmup: int):
                 block_table=pin(case.block_table), rms_norm_weight=pin(case.rms_norm_weight),
                 cos_sin_cache=pin(case.cos_sin_cache), kv_slot_mapping=pin(case.kv_slot_mapping),
                 kv_cache=pin(case.kv_cache))
-    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-    out = torch.empty_like(host["kv_cache"]).pin_memory()
+    devs = [{k: torch.empty_like(v, device=device) for k, v in host.items()} for _ in range(2)]
+    outs = [torch.empty_like(host["kv_cache"]).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out.numel() * out.element_size()
-    stream = torch.cuda.Stream(device)
+    d2h = outs[0].numel() * outs[0].element_size()
+    copy_s = torch.cuda.Stream(device)
+    comp_s = torch.cuda.Stream(device)
     ws = torch.zeros(kvc.kvc_workspace_bytes(case.num_outputs), dtype=torch.uint8, device=device)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
-        kvc.c128_256_512_compress(block_size=case.block_size, compress_ratio=case.compress_ratio,
-                                  rms_norm_eps=case.rms_norm_eps, stream=stream, workspace=ws,
-                                  **dev)
-        out.copy_(dev["kv_cache"], non_blocking=True)
+    def step(i):
+        b = i % 2
+        dev = devs[b]
+        with torch.cuda.stream(copy_s):
+            if i >= 2:
+                copy_s.wait_event(done[b])
+            for k in host:
+                dev[k].copy_(host[k], non_blocking=True)
+            copied[b].record(copy_s)
+        with torch.cuda.stream(comp_s):
+            comp_s.wait_event(copied[b])
+            kvc.c128_256_512_compress(block_size=case.block_size,
+                                      compress_ratio=case.compress_ratio,
+                                      rms_norm_eps=case.rms_norm_eps, stream=comp_s,
+                                      workspace=ws, **dev)
+            outs[b].copy_(dev["kv_cache"], non_blocking=True)
+            done[b].record(comp_s)
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, warmup)):
-            step()
-        stream.synchronize()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        barrier()
-        ev0.record(stream)
-        for _ in range(steps):
-            step()
-        ev1.record(stream)
-        stream.synchronize()
+    for i in range(max(3, warmup)):
+        step(i)
+    torch.cuda.synchronize(device)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(copy_s)
+    comp_s.wait_event(ev0)
+    for i in range(steps):
+        step(i)
+    copy_s.wait_stream(comp_s)
+    ev1.record(copy_s)
+    torch.cuda.synchronize(device)
     elapsed = ev0.elapsed_time(ev1) / 1e3
-    assert np.array_equal(out.numpy().shape, case.kv_cache.shape)
+    assert outs[0].shape == host["kv_cache"].shape
     return elapsed / steps, h2d, d2h
 
 
