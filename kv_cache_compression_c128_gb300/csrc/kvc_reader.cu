@@ -319,9 +319,9 @@ namespace {
 //   us; either change alone gained at most 3.5 %; 6 and 12 slots were slower);
 // bf16 output: 2 slots per warp and pass, plain stores (79.2 -> 76.8 us;
 //   streaming stores or more slots made it 4-27 % slower).
-#define KVC_WARP_F32 kvc_dequant_warp_kernel<8, true>
-#define KVC_WARP_BF16 kvc_dequant_warp_kernel<2, false>
-#define KVC_WIDE16_BF16 kvc_dequant_wide16_kernel<2>
+constexpr auto kWarpF32 = &kvc_dequant_warp_kernel<8, true>;
+constexpr auto kWarpBf16 = &kvc_dequant_warp_kernel<2, false>;
+constexpr auto kWide16Bf16 = &kvc_dequant_wide16_kernel<2>;
 
 // CTAs of a kernel that fit on the current device at once (cached per device).
 int resident_ctas(int dev, const void* kernel, std::atomic<int>* cache) {
@@ -348,9 +348,9 @@ cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   const void* small_fn = reinterpret_cast<const void*>(&kvc_dequant_kernel<1>);
   const bool wide16 = out_bf16 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
-  const void* large_fn = wide16     ? reinterpret_cast<const void*>(&KVC_WIDE16_BF16)
-                         : out_bf16 ? reinterpret_cast<const void*>(&KVC_WARP_BF16)
-                                    : reinterpret_cast<const void*>(&KVC_WARP_F32);
+  const void* large_fn = wide16     ? reinterpret_cast<const void*>(kWide16Bf16)
+                         : out_bf16 ? reinterpret_cast<const void*>(kWarpBf16)
+                                    : reinterpret_cast<const void*>(kWarpF32);
   const int cap_s = resident_ctas(dev, small_fn, small_cap);
   const int cap_l = resident_ctas(dev, large_fn, wide16 ? wide_cap : out_bf16 ? bf16_cap : f32_cap);
   if (cap_s == 0 || cap_l == 0) return cudaErrorInvalidDevice;
@@ -373,12 +373,12 @@ cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_
     e = cudaLaunchKernelEx(&cfg, &kvc_dequant_kernel<1>, kv, num_pages, slots, num_slots, out,
                            out_bf16, err);
   } else if (wide16) {
-    e = cudaLaunchKernelEx(&cfg, &KVC_WIDE16_BF16, kv, num_pages, slots, num_slots,
+    e = cudaLaunchKernelEx(&cfg, kWide16Bf16, kv, num_pages, slots, num_slots,
                            static_cast<uint16_t*>(out), err);
   } else if (out_bf16) {
-    e = cudaLaunchKernelEx(&cfg, &KVC_WARP_BF16, kv, num_pages, slots, num_slots, out, out_bf16, err);
+    e = cudaLaunchKernelEx(&cfg, kWarpBf16, kv, num_pages, slots, num_slots, out, out_bf16, err);
   } else {
-    e = cudaLaunchKernelEx(&cfg, &KVC_WARP_F32, kv, num_pages, slots, num_slots, out, out_bf16, err);
+    e = cudaLaunchKernelEx(&cfg, kWarpF32, kv, num_pages, slots, num_slots, out, out_bf16, err);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
