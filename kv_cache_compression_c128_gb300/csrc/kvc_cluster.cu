@@ -17,22 +17,24 @@
 // 96 KiB ring of 32 KiB stages either way.  Output n is handled by one
 // thread-block cluster of S CTAs (S = 1, 2, 4, 8, 16); rank j streams chunks
 // [j K/S, (j+1) K/S).  Persistent clusters take contiguous, equal ranges of
-// outputs, so every CTA streams the same number of chunks.  A multi-layer call simply has L * N outputs: output o is
-// window o mod N of layer o / N (same chunks, that layer's state cache,
-// weight and kv_cache), so all layers share one launch and one balanced
-// split.
+// outputs, so every CTA streams the same number of chunks.  A multi-layer
+// call simply has L * N outputs: output o is window o mod N of layer o / N
+// (same chunks, that layer's state cache, weight and kv_cache), so all
+// layers share one launch and one balanced split.
 //
 // Inside a CTA (320 threads):
 //   warp 9  resolver: turns units into physical blocks (boundary index ->
 //           request/position/slot -> block_table) 32 at a time, two chunks
 //           ahead, into a shared-memory FIFO;
-//   warp 8  issuer: one cp.async.bulk per run of rows (one per row when the
-//           rows of a block are not adjacent) into a ring of three 32 KiB
-//           stages (two bf16 chunks or one fp32 chunk each), each stage
-//           guarded by a full/empty mbarrier pair;
+//   warp 8  issuer: one cp.async.bulk per run of rows into a ring of three
+//           32 KiB stages (two bf16 chunks or one fp32 chunk each), each
+//           stage guarded by a full/empty mbarrier pair.  When the rows of a
+//           block are not adjacent: one TMA tensor copy per chunk through a
+//           per-layer tensor map, or one bulk copy per row without one;
 //   warps 0-7 consumers: thread t owns dims 2t, 2t+1 and folds every staged
 //           chunk into its (max, denominator, numerator), a stage of two
-//           full bf16 chunks as 16 rows with one rescale.
+//           full bf16 chunks as 16 rows with one rescale.  Before the grid
+//           dependency wait, warp 0 warms L2 with the CTA's first stages.
 // With S = 1 the consumers then finalise the output directly.  With S > 1
 // every rank pushes its partial state to the finaliser rank owning each dim
 // (F = min(S, 8) finalisers, 512/F dims each) with st.async, which completes
