@@ -37,10 +37,10 @@ def kvc():
     return kvc
 
 
-def _draw(seed):
+def _draw(seed, block_sizes=(8, 16, 24, 32, 64)):
     rng = np.random.Generator(np.random.PCG64(seed))
     R = int(rng.integers(1, 5))
-    B = int(rng.choice([8, 16, 24, 32, 64]))
+    B = int(rng.choice(list(block_sizes)))
     C = int(rng.choice([1, 2, 7, 8, 13, 16, 31, 64, 100, 128, 256, 300, 512, 600]))
     per_req = max(C, B)
     lengths = [B * int(np.ceil((per_req + int(rng.integers(0, 4 * B + 200))) / B)) for _ in range(R)]
@@ -74,9 +74,20 @@ def _draw(seed):
     return case, slots, f32, row_pad, block_pad, table, route, count, row_copies
 
 
-@pytest.mark.parametrize("seed", range(4000, 4120))
+@pytest.mark.parametrize("seed", range(4000, 4200))
 def test_random_configuration(kvc, oracle_mod, seed):
-    case, slots, f32, row_pad, block_pad, table, route, count, row_copies = _draw(seed)
+    _check_draw(kvc, oracle_mod, seed, _draw(seed))
+
+
+@pytest.mark.parametrize("seed", range(5000, 5060))
+def test_random_configuration_blocks_not_multiple_of_8(kvc, oracle_mod, seed):
+    # block sizes that are not a multiple of 8: most chunks straddle two
+    # blocks, with rows apart copied row by row around the tensor copies
+    _check_draw(kvc, oracle_mod, seed, _draw(seed, (9, 12, 20, 40, 100)))
+
+
+def _check_draw(kvc, oracle_mod, seed, draw):
+    case, slots, f32, row_pad, block_pad, table, route, count, row_copies = draw
     state = inputs.fp32_state(case.num_state_blocks, case.block_size, seed + 1) if f32 \
         else case.state_bits
     G, B, _ = state.shape
