@@ -67,3 +67,32 @@ def test_single_process_reduction_is_identity():
 
     assert bench.max_over_ranks(1.5) == 1.5
     assert bench.rank_seed(7, 0) == 7
+
+
+def test_threaded_oracle_timing_writes_the_single_threaded_bytes():
+    # the all-cores CPU baseline runs the unchanged oracle on slices of the
+    # outputs in several threads at once; the slices write disjoint slots, so
+    # the cache must come out byte for byte as one single-threaded call leaves it
+    import sys
+
+    import numpy as np
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import bench
+    import oracle
+    from kv_cache_compression_c128_gb300 import inputs
+
+    case = inputs.make_case(2, 2048, 64, seed=inputs.BASE_SEED + 6000, kv_fill=9)
+    kvs = []
+    _, n = bench.time_oracle_threads(case, 5, min_seconds=1e9, max_passes=2, kv_out=kvs)
+    assert n == 2 * case.num_outputs and len(kvs) == 1
+    kv1 = case.kv_cache.copy()
+    res = oracle.compress(case.state_bits, case.token_to_req, case.positions,
+                          case.boundary_token_indices, case.block_table, case.rms_norm_weight,
+                          case.cos_sin_cache, case.kv_slot_mapping, kv1, case.block_size,
+                          case.compress_ratio, case.rms_norm_eps)
+    assert res["status"] == 0
+    assert np.array_equal(kvs[0], kv1)
+    assert not np.array_equal(kv1, case.kv_cache)
