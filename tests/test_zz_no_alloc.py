@@ -107,33 +107,3 @@ def test_static_entry_refuses_problems_beyond_its_buffer(kvc):
     st = kvc.kvc_compress_static(*args)
     assert st == kvc.KVC_ERR_SCRATCH_LIMIT
     assert "8 MiB" in kvc.kvc_error_string(st)
-
-
-def test_static_entry_in_a_cuda_graph(kvc):
-    # the per-call counter reset (cudaMemsetAsync) and the launch are both
-    # stream work, so the call can be captured and replayed; its first call on
-    # the device (the symbol lookup) is made before the capture
-    case = inputs.make_case(2, 4096, 128, seed=inputs.BASE_SEED + 4300, kv_fill=6)
-    d = to_device(case)
-    N = case.num_outputs
-    stream = torch.cuda.Stream()
-    sp = stream.cuda_stream
-    flags = kvc.make_flags("streamk")
-    y = torch.zeros((N, 512), dtype=torch.float32, device="cuda")
-    with torch.cuda.stream(stream):
-        assert kvc.kvc_compress_static(*_raw_args(d, case, y, sp), flags, sp) == kvc.KVC_OK
-        stream.synchronize()
-        kv_ref = d["kv_cache"].cpu().numpy()
-        y_ref = y.cpu().numpy()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            st = kvc.kvc_compress_static(*_raw_args(d, case, y, sp), flags, sp)
-        assert st == kvc.KVC_OK
-        for _ in range(2):
-            d["kv_cache"].copy_(torch.from_numpy(case.kv_cache))
-            y.zero_()
-            g.replay()
-            stream.synchronize()
-            assert kvc.kvc_get_device_error(sp) == 0
-            assert np.array_equal(d["kv_cache"].cpu().numpy(), kv_ref)
-            assert np.array_equal(y.cpu().numpy(), y_ref)
