@@ -5,10 +5,13 @@ may start while the previous kernel on the stream is still running, and it
 warms L2 with its first stages, from the index arrays as they stand, before
 its grid dependency wait.  Only loads after the wait may reach a result.
 
-Here call A writes its y output, and call B, queued right behind it on the
-same stream, reads that same memory as its fp32 state.  B must produce
-exactly what it produces when the host synchronises between the two calls,
-and not what it produced on the buffer's earlier contents.
+In the first test call A writes its y output, and call B, queued right
+behind it on the same stream, reads that same memory as its fp32 state; in
+the second, B reads A's packed slots as its positions array.  B must
+produce exactly what it produces when the host synchronises between the two
+calls, and not what it produced on the buffer's earlier contents.  B's
+outputs are allocated before A is queued, so that no other kernel or copy
+sits between the two on the stream.
 """
 import numpy as np
 import pytest
@@ -56,9 +59,13 @@ def test_call_reads_the_previous_calls_output(kvc, route):
     def run_a():
         kvc.c128_256_512_compress(a_state, block_size=8, compress_ratio=16, y_out=y, **a_args)
 
-    def run_b():
-        kv = b_args["kv_cache"].clone()
-        yb = torch.zeros((b.num_outputs, 512), dtype=torch.float32, device="cuda")
+    def out_b():
+        # B's outputs are made before A is queued: any kernel or copy between
+        # A and B on the stream would keep B from starting inside A
+        return (b_args["kv_cache"].clone(),
+                torch.zeros((b.num_outputs, 512), dtype=torch.float32, device="cuda"))
+
+    def run_b(kv, yb):
         kvc.c128_256_512_compress(b_state, block_size=8, compress_ratio=64, y_out=yb, flags=flags,
                                   **dict(b_args, kv_cache=kv))
         return kv, yb
@@ -66,21 +73,96 @@ def test_call_reads_the_previous_calls_output(kvc, route):
     # stale contents first, read once by B so that its lines sit in the caches
     y.copy_(torch.randn_like(y))
     torch.cuda.synchronize()
-    kv_stale, y_stale = run_b()
+    kv_stale, y_stale = run_b(*out_b())
     torch.cuda.synchronize()
     # A then B back to back on one stream: B may start before A ends
     for _ in range(3):
+        outs = out_b()
         run_a()
-        kv_chain, y_chain = run_b()
+        kv_chain, y_chain = run_b(*outs)
         torch.cuda.synchronize()
         assert kvc.kvc_get_device_error(torch.cuda.current_stream().cuda_stream) == 0
         # the same with the host waiting for A before B is queued
-        kv_sync, y_sync = run_b()
+        kv_sync, y_sync = run_b(*out_b())
         torch.cuda.synchronize()
         assert torch.equal(kv_chain, kv_sync)
         assert torch.equal(y_chain.view(torch.int32), y_sync.view(torch.int32))
         assert not torch.equal(y_chain, y_stale)
         y.copy_(torch.randn_like(y))  # stale again for the next round
         torch.cuda.synchronize()
-        run_b()
+        run_b(*out_b())
         torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("route", ["auto", "s2"])
+def test_call_reads_its_positions_from_the_previous_calls_slots(kvc, route):
+    # Before its grid dependency wait the kernel resolves its first chunks
+    # from the index arrays as they stand, to warm L2; only what it loads
+    # after the wait may reach a result.  Here call B's positions array IS
+    # call A's kv_cache, so B's early pass can see positions A has not
+    # written yet, and B must still produce what it produces after A is done.
+    #
+    # A: 512 windows whose values are exactly 1 in dims d = 0 mod 8 (d < 448)
+    # and 0 elsewhere, unit weights.  Then c is exactly that 0/1 pattern
+    # (every sum of a softmax weight times 1 equals the matching denominator
+    # term), and each of A's 64-dim groups codes to q at dims 0 mod 8 and 0
+    # elsewhere: every 8-byte word of a code region reads as the int64 q.
+    a = inputs.make_case(8, 65536, 128, seed=inputs.BASE_SEED + 7100)
+    cols = np.arange(512)
+    vals = np.where((cols % 8 == 0) & (cols < 448), 0x3F80, 0).astype(np.uint16)
+    a.state_bits[:, :, :512] = vals
+    a.rms_norm_weight[:] = 1.0
+    a_state, a_args = _dev(a)
+    a_kv = a_args["kv_cache"]
+    words = a_kv.view(-1).view(torch.int64)                # B's positions [pages * 4672]
+    # B: windows of 16 rows in one request of 16 blocks, at the positions held
+    # by 256 code words of A's slots (word m of slot s: page*4672 + off*72 + m)
+    rng = np.random.Generator(np.random.PCG64(inputs.BASE_SEED + 7101))
+    slots = rng.choice(a.num_outputs, size=256, replace=True)
+    m = rng.integers(0, 56, size=256)
+    bti = np.unique((slots // 64) * 4672 + (slots % 64) * 72 + m)
+    n_b = bti.size
+    t_b = words.numel()
+    b_state = torch.from_numpy(
+        inputs.make_case(1, 128, 16, seed=inputs.BASE_SEED + 7102).state_bits.view(np.int16)
+    ).view(torch.bfloat16).cuda()
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    b_args = dict(token_to_req=torch.zeros(t_b, dtype=torch.int32, device="cuda"),
+                  positions=words, boundary_token_indices=t(bti.astype(np.int64)),
+                  block_table=t(rng.permutation(16).astype(np.int32)[None, :]),
+                  rms_norm_weight=t(a.rms_norm_weight), cos_sin_cache=t(inputs._cos_sin_table(128)),
+                  kv_slot_mapping=t(rng.permutation(n_b).astype(np.int64)))
+    flags = 0 if route == "auto" else kvc.make_flags("cluster", 0, 2)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def run_a():
+        kvc.c128_256_512_compress(a_state, block_size=8, compress_ratio=128, **a_args)
+
+    def out_b():  # made before A is queued, so that B directly follows A
+        return (torch.zeros((4, inputs.KV_PAGE_BYTES), dtype=torch.uint8, device="cuda"),
+                torch.zeros((n_b, 512), dtype=torch.float32, device="cuda"))
+
+    def run_b(kv, yb):
+        kvc.c128_256_512_compress(b_state, block_size=8, compress_ratio=16, y_out=yb,
+                                  flags=flags, kv_cache=kv, **b_args)
+        return kv, yb
+
+    run_a()
+    torch.cuda.synchronize()
+    q = words[torch.from_numpy(bti).cuda()]
+    assert int(q.min()) >= 63 and int(q.max()) <= 127, "A's code words"
+    kv_sync, y_sync = run_b(*out_b())
+    torch.cuda.synchronize()
+    assert kvc.kvc_get_device_error(stream) == 0
+    for _ in range(3):
+        words.fill_(40)                                    # another valid position
+        kv_stale, _ = run_b(*out_b())                      # B on the stale positions
+        torch.cuda.synchronize()
+        assert not torch.equal(kv_stale, kv_sync)
+        outs = out_b()
+        run_a()
+        kv_chain, y_chain = run_b(*outs)                   # queued right behind A
+        torch.cuda.synchronize()
+        assert kvc.kvc_get_device_error(stream) == 0
+        assert torch.equal(kv_chain, kv_sync)
+        assert torch.equal(y_chain.view(torch.int32), y_sync.view(torch.int32))
