@@ -469,12 +469,15 @@ __device__ void prefetch_first_stages(const Params& p, int64_t n0, int64_t units
   ChunkRuns cr;
   MetaRec rec;
   resolve_chunk_t<true>(p, o - static_cast<int64_t>(layer) * p.num_outputs, k_lo + kk, false, cr, rec);
-  // How much to prefetch, as measured: the first two of the three stages.
-  // The whole first pass made calls with no earlier grid to overlap 1.5-2 us
-  // slower (its prefetches queue ahead of the real copies), and one stage
-  // gains less.  Rows apart without a map take one prefetch per row: the
-  // first stage alone.
-  const int first = (p.rows_contiguous || maps ? kStages - 1 : 1) * T::kChunksPerStage;
+  // How much to prefetch, as measured on the bf16 shapes: the ring's first
+  // pass, i.e. the chunks the issuer copies before it first waits for a
+  // free stage.  Against two stages this took 0.5 % off the headline in
+  // graph replay and cost some mid-size calls with no earlier grid to
+  // overlap about 1 us (their prefetches queue ahead of the real copies);
+  // ten chunks, past the ring, were slower both ways (up to 4.5 % in replay
+  // and 10 % cold on the 64 MiB shapes).  Rows apart without a map take
+  // one prefetch per row: the first stage alone.
+  const int first = (p.rows_contiguous || maps ? T::kNumStages : 1) * T::kChunksPerStage;
   if (cr.off1 < 0 || lane >= first) return;
   const uint8_t* state = p.states[layer];
   if (p.rows_contiguous) {
