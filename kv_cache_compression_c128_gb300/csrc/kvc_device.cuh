@@ -215,6 +215,17 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of a cluster barrier, for a thread that has work to do in
+// between.  Every thread of the cluster arrives once, then waits once,
+// before it arrives again.  The relaxed arrive publishes mbarrier
+// initialisation when fence_mbar_init() came before it.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ---- bf16 and float helpers -----------------------------------------------------
 
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
