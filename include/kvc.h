@@ -25,6 +25,22 @@
  * All pointers name device memory of the current CUDA device unless stated
  * otherwise; the caller owns every buffer.  Calls are asynchronous on the
  * given stream and never synchronise it (kvc_get_device_error excepted).
+ * The library's own per-device set-up (kernel attributes, the addresses of
+ * its device-side words) is made at the first call in a CUDA context and made
+ * again when another context is current on that device, e.g. after
+ * cudaDeviceReset.
+ *
+ * Two choices of this interface that a reader of the statement's signature
+ * might not expect:
+ *   - Index checking is always on: every index is range-checked on its way
+ *     to an address, and a bad one is reported through kvc_get_device_error.
+ *     There is no "checked mode" flag.  The low 16 bits of `flags` force the
+ *     launch size instead (see below): flags = 1 runs the whole call on ONE
+ *     cluster, which computes the same bytes but many times slower.  Pass 0.
+ *   - kvc_compress does not allocate.  Scratch for outputs whose window is
+ *     split between CTAs is a caller-owned, zero-filled workspace
+ *     (kvc_workspace_bytes); the Python binding keeps one per device and
+ *     stream.  kvc_compress_static uses a buffer inside the library instead.
  */
 #ifndef KVC_H_
 #define KVC_H_
@@ -53,9 +69,11 @@ typedef enum {
 } kvc_status;
 
 /*
- * flags (0 = automatic choice of everything):
+ * flags (0 = automatic choice of everything; use 0 outside tuning and tests):
  *   bits 0..15   force the launch size: clusters for the cluster route, CTAs
  *                for the stream-K route (capped at what fits on the device);
+ *                NOT a "checked mode" switch -- checking is always on, and
+ *                flags = 1 forces a single cluster;
  *   bits 16..20  force the cluster size S (1, 2, 4, 8 or 16, at most C/8);
  *   bit 24       use the stream-K route instead of the cluster route;
  *   bit 25       rows apart (kvc_compress_strided): copy one row at a time
@@ -121,7 +139,14 @@ size_t kvc_workspace_bytes(int64_t num_outputs);
  * errors (an index outside its array, a window that starts before position
  * 0 or off an 8-row block boundary) never trap: the offending output's slot
  * is left untouched, the other outputs are written, and a sticky device
- * error code is recorded for kvc_get_device_error.
+ * error code is recorded for kvc_get_device_error.  Every wait of the
+ * kernels is bounded: a wait that runs past its limit records
+ * KVC_ERR_TIMEOUT, the kernel stops issuing copies, waits for the ones in
+ * flight and returns.  When a pipeline wait (a copy stage, a hand-off
+ * between warps) ran out, every slot is either written whole, with the bytes
+ * an undisturbed call writes, or left untouched; when an exchange between
+ * the CTAs of a cluster ran out (a peer that stopped answering), the slots
+ * of the outputs that exchange served are unspecified.
  */
 kvc_status kvc_compress(
     const void* state_cache, int64_t num_state_blocks,
@@ -271,11 +296,14 @@ kvc_status kvc_dequantize(const uint8_t* kv_cache, int64_t num_kv_pages,
  * Scratch comes from an 8 MiB buffer inside the library (a file-scope
  * __device__ array, held by every device that loads the library until the
  * process exits).  Nothing is allocated: no cudaMalloc, no cudaFree, no
- * allocating library routine.  The first call on a device looks up the
- * buffer's device address (cudaGetSymbolAddress) and sets up the kernel for
- * that device; make that first call before any stream capture on the device.
- * Each call clears the buffer's arrival counters with cudaMemsetAsync on
- * `stream`, then computes exactly what kvc_compress computes.
+ * allocating library routine.  The first call on a device (and the first
+ * after the device's context changed, e.g. after cudaDeviceReset) looks up
+ * the buffer's device address (cudaGetSymbolAddress) and sets up the kernel
+ * for that device; make that first call before any stream capture on the
+ * device.  Once every argument check has passed, each call clears the
+ * buffer's arrival counters with cudaMemsetAsync on `stream`, then computes
+ * exactly what kvc_compress computes; a call refused by a check writes
+ * nothing.
  *
  * Every call on a device shares the one buffer, which keeps the last call's
  * contents: calls that overlap on the GPU (different streams, not ordered by
@@ -330,6 +358,24 @@ kvc_status kvc_query_launch_ex(int64_t num_outputs, int32_t compress_ratio,
  * context stays usable.  KVC_ERR_INVALID_ARG for a limit outside the range.
  */
 kvc_status kvc_selftest_wait_timeout(uint64_t limit_cycles, void* stream);
+
+/*
+ * Test hook for the kernels' abort path: sets the limit, in SM clock cycles,
+ * on each pipeline wait (a copy stage, a hand-off between warps) of every
+ * compression launched afterwards by this process, on any device.
+ * limit_cycles 0 restores the default (4e9 cycles, about 2 s); 1 .. 4e9 sets
+ * it; larger values return KVC_ERR_INVALID_ARG.  Limits below 100000 cycles
+ * are polled without suspending the waiting thread, so they run out on time.
+ * A short limit makes real calls give up part way: each records
+ * KVC_ERR_TIMEOUT, stops issuing copies, drains the copies already in flight
+ * (that drain, and the exchanges between the CTAs of a cluster, keep the
+ * default limit, so no CTA exits while a copy or a peer may still write into
+ * it) and returns, with every slot either written whole or untouched.  It
+ * exists so that this path can be tested on real launches; production
+ * callers never need it.  Not synchronised with calls in flight on other
+ * host threads.
+ */
+kvc_status kvc_selftest_set_wait_limit(uint64_t limit_cycles);
 
 /*
  * Synchronises `stream`, then reads and clears the device error code

@@ -162,6 +162,8 @@ def lib():
             L.kvc_query_launch_ex.restype = ctypes.c_int
             L.kvc_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
             L.kvc_selftest_wait_timeout.restype = ctypes.c_int
+            L.kvc_selftest_set_wait_limit.argtypes = [ctypes.c_uint64]
+            L.kvc_selftest_set_wait_limit.restype = ctypes.c_int
             L.kvc_get_device_error.argtypes = [P, P]
             L.kvc_get_device_error.restype = ctypes.c_int
             L.kvc_error_string.argtypes = [ctypes.c_int]
@@ -213,6 +215,13 @@ def kvc_selftest_wait_timeout(limit_cycles: int, stream: Optional[int] = None) -
     """Launch the bounded-wait self-test (a wait that runs out after
     limit_cycles and records KVC_ERR_TIMEOUT); returns the launch status."""
     return int(lib().kvc_selftest_wait_timeout(int(limit_cycles), ctypes.c_void_p(stream or 0)))
+
+
+def kvc_selftest_set_wait_limit(limit_cycles: int) -> int:
+    """Test hook: the limit (SM cycles) on each pipeline wait of later
+    compressions in this process; 0 restores the default.  Returns the
+    status."""
+    return int(lib().kvc_selftest_set_wait_limit(int(limit_cycles)))
 
 
 def kvc_get_device_error(stream: Optional[int] = None) -> int:

@@ -3,14 +3,54 @@
 // cluster route (kvc_cluster.cu) and the stream-K route (kvc_streamk.cu),
 // workspace sizing and device error reporting.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/kvc.h"
 #include "kvc_internal.h"
+
+namespace {
+
+// Limit on one pipeline wait of the kernels, in SM clock cycles: the default
+// unless kvc_selftest_set_wait_limit shortened it.
+std::atomic<long long> g_wait_limit{kvc::kDefaultWaitLimitCycles};
+
+// A driver entry point looked up through the runtime (no link against the
+// driver library); null when the driver does not offer it.
+template <typename Fn>
+Fn driver_entry(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return reinterpret_cast<Fn>(f);
+}
+
+}  // namespace
+
+namespace kvc {
+
+unsigned long long context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static const GetCurrent get_current = driver_entry<GetCurrent>("cuCtxGetCurrent");
+  static const GetId get_id = driver_entry<GetId>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  if (get_current == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id != nullptr && get_id(ctx, &id) == CUDA_SUCCESS) return id + 1;  // never 0
+  return static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(ctx));
+}
+
+}  // namespace kvc
 
 namespace {
 
@@ -25,6 +65,7 @@ constexpr int kNumClusterSizes = 5;
 
 struct DeviceInfo {
   bool ready = false;
+  unsigned long long ctx = 0;  // context the set-up was made in (kvc::context_id)
   int sms = 0;
   int streamk_ctas_per_sm = 0;
   int cluster_cap[kNumClusterSizes] = {};  // co-resident clusters per size
@@ -35,13 +76,18 @@ std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 
 // Per-device set-up on first use (with that device current): shared-memory
-// opt-in and occupancy of both routes, address of the error word.
+// opt-in and occupancy of both routes, address of the error word.  All of it
+// belongs to the CUDA context it was made in; when another context is
+// current (after cudaDeviceReset, or a context the caller created), the
+// set-up is made again.
 kvc_status device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_ERR_CUDA;
+  const unsigned long long ctx = kvc::context_id();
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceInfo& d = g_devices[dev];
-  if (!d.ready) {
+  if (!d.ready || ctx == 0 || d.ctx != ctx) {
+    d.ready = false;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return KVC_ERR_CUDA;
@@ -61,6 +107,7 @@ kvc_status device_info(DeviceInfo* out) {
     d.sms = sms;
     d.streamk_ctas_per_sm = per_sm;
     d.error_word = static_cast<uint32_t*>(err);
+    d.ctx = kvc::context_id();  // the set-up's runtime calls made a context current
     d.ready = true;
   }
   *out = d;
@@ -220,7 +267,8 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, const Sta
                            const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
                            uint8_t* const* kv_caches, int64_t num_kv_pages, int32_t block_size,
                            int32_t compress_ratio, float rms_norm_eps, float* y_out,
-                           void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+                           void* workspace, size_t workspace_bytes, uint32_t flags, void* stream,
+                           const kvc::PreLaunch* pre_launch = nullptr) {
   if (num_outputs < 0 || (flags & ~KVC_FLAG_ALL) != 0) return KVC_ERR_INVALID_ARG;
   if (L < 1 || L > kvc::kMaxLayers) return KVC_ERR_INVALID_ARG;
   if (lay.dtype != KVC_DTYPE_BF16 && lay.dtype != KVC_DTYPE_F32) return KVC_ERR_INVALID_ARG;
@@ -303,6 +351,7 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, const Sta
   p.part_status = reinterpret_cast<int32_t*>(ws + WL.status);
   p.counters = reinterpret_cast<int32_t*>(ws + WL.counters);
   p.error = d.error_word;
+  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
 
   const bool streamk_ok = lay.dtype == KVC_DTYPE_BF16 && p.rows_contiguous &&
                           block_size == kvc::kBlockRows && compress_ratio % kvc::kBlockRows == 0;
@@ -320,6 +369,7 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, const Sta
     p.use_maps = ok ? 1 : 0;
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pre_launch != nullptr && pre_launch->fn(pre_launch->ctx, s) != cudaSuccess) return KVC_ERR_CUDA;
   if (!r.stream_k) return kvc::launch_cluster(p, r.count, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
   // stream-K: one launch per layer (each reuses the workspace, in stream order)
   const int ctas =
@@ -337,6 +387,30 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, const Sta
 }
 
 }  // namespace
+
+namespace kvc {
+
+kvc_status compress_hooked(const void* state_cache, int64_t num_state_blocks,
+                           const int32_t* token_to_req, const int64_t* positions,
+                           int64_t num_tokens, const int64_t* boundary_token_indices,
+                           int64_t num_outputs, const int32_t* block_table, int64_t num_reqs,
+                           int64_t max_blocks_per_req, const float* rms_norm_weight,
+                           const float* cos_sin_cache, int64_t num_positions,
+                           const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+                           uint8_t* kv_cache, int64_t num_kv_pages, int32_t block_size,
+                           int32_t compress_ratio, float rms_norm_eps, float* y_out,
+                           void* workspace, size_t workspace_bytes, uint32_t flags, void* stream,
+                           const PreLaunch* pre_launch) {
+  return compress_layers(1, &state_cache, contiguous_layout(block_size, max_blocks_per_req),
+                         num_state_blocks, token_to_req, positions, num_tokens,
+                         boundary_token_indices, num_outputs, block_table, num_reqs,
+                         max_blocks_per_req, &rms_norm_weight, cos_sin_cache, num_positions,
+                         kv_slot_mapping, slot_mapping_len, &kv_cache, num_kv_pages, block_size,
+                         compress_ratio, rms_norm_eps, y_out, workspace, workspace_bytes, flags,
+                         stream, pre_launch);
+}
+
+}  // namespace kvc
 
 extern "C" {
 
@@ -448,6 +522,14 @@ kvc_status kvc_selftest_wait_timeout(uint64_t limit_cycles, void* stream) {
   const cudaError_t e = kvc::launch_selftest_wait(static_cast<long long>(limit_cycles),
                                                   d.error_word, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+kvc_status kvc_selftest_set_wait_limit(uint64_t limit_cycles) {
+  if (limit_cycles > static_cast<uint64_t>(kvc::kDefaultWaitLimitCycles)) return KVC_ERR_INVALID_ARG;
+  g_wait_limit.store(limit_cycles == 0 ? kvc::kDefaultWaitLimitCycles
+                                       : static_cast<long long>(limit_cycles),
+                     std::memory_order_relaxed);
+  return KVC_OK;
 }
 
 kvc_status kvc_get_device_error(void* stream, uint32_t* out_code) {

@@ -146,7 +146,7 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, int64_t n0, int6
     const uint32_t ph = static_cast<uint32_t>((c >> 1) & 1);
     bool ok = true;
     if (lane == 0) {
-      ok = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.fifo_empty[h], ph ^ 1u);
+      ok = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.fifo_empty[h], ph ^ 1u, p.wait_limit);
       if (!ok && !aborted(&sh.abort_flag)) {
         record_error(p.error, kErrTimeout);
         set_abort(&sh.abort_flag);
@@ -196,7 +196,7 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
     const uint32_t ph = static_cast<uint32_t>((c >> 1) & 1);
     bool ok = true;
     if (lane == 0) {
-      ok = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.fifo_full[h], ph);
+      ok = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.fifo_full[h], ph, p.wait_limit);
       if (!ok && !aborted(&sh.abort_flag)) {
         record_error(p.error, kErrTimeout);
         set_abort(&sh.abort_flag);
@@ -211,7 +211,7 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
       if (half == 0) {
         bool free = true;
         if (lane == 0) {
-          free = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u);
+          free = !aborted(&sh.abort_flag) && mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u, p.wait_limit);
           if (!free && !aborted(&sh.abort_flag)) {
             record_error(p.error, kErrTimeout);
             set_abort(&sh.abort_flag);
@@ -292,7 +292,7 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
   // No bulk copy may still target this CTA's shared memory when it exits.
   for (int s = 0; s < T::kNumStages; ++s)
     if ((issued >> s) & 1u)
-      if (!mbar_wait_bounded(&sh.full_bar[s], (last_parity >> s) & 1u)) record_error(p.error, kErrTimeout);
+      if (!mbar_wait_drain(&sh.full_bar[s], (last_parity >> s) & 1u)) record_error(p.error, kErrTimeout);
 }
 
 // cluster_waited: whether this thread has completed the start-up cluster
@@ -334,7 +334,7 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
     for (int kk = 0; kk < kj; kk += T::kChunksPerStage) {
       bool ready = false;
       if (!aborted(&sh.abort_flag)) {
-        ready = mbar_wait_bounded(&sh.full_bar[stage], phase);
+        ready = mbar_wait_bounded(&sh.full_bar[stage], phase, p.wait_limit);
         if (!ready) {
           record_error(p.error, kErrTimeout);
           set_abort(&sh.abort_flag);

@@ -20,7 +20,7 @@ namespace dev {
 constexpr uint32_t kErrUnsupported = 2;
 constexpr uint32_t kErrBadIndex = 4;
 constexpr uint32_t kErrTimeout = 5;
-constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr long long kWaitLimitCycles = kDefaultWaitLimitCycles;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Slot record of one output piece, handed from the copy-issuing warp to the
@@ -75,10 +75,35 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
   return done != 0;
 }
 
+// Non-blocking probe of the phase of `bar` with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Limits below this many cycles are polled with test_wait and the clock read
+// after every probe: a try_wait may suspend the thread for a hardware-chosen
+// time that can exceed such a limit.  (Only the test hook that shortens the
+// pipeline waits asks for limits this short.)
+constexpr long long kPollBelowCycles = 100000;
+
 // Wait for the phase of `bar` with the given parity; false once more than
 // `limit` SM clock cycles have passed.
 static __device__ __noinline__ bool mbar_wait_bounded_for(unsigned long long* bar, uint32_t parity,
                                                           long long limit) {
+  if (limit < kPollBelowCycles) {
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity))
+      if (clock64() - t0 > limit) return false;
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -88,8 +113,17 @@ static __device__ __noinline__ bool mbar_wait_bounded_for(unsigned long long* ba
   }
 }
 
-// The pipelines' wait: mbar_wait_bounded_for with the kernels' limit.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
+// A pipeline wait (a stage, a FIFO half): bounded by the call's limit
+// (Params::wait_limit; kWaitLimitCycles unless a test shortened it).
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
+                                                  long long limit) {
+  return mbar_wait_bounded_for(bar, parity, limit);
+}
+
+// The final drain of a CTA's own bulk copies always takes the long limit: a
+// CTA must not exit while a copy may still write into its shared memory, and
+// a copy of valid addresses always lands.
+__device__ __forceinline__ bool mbar_wait_drain(unsigned long long* bar, uint32_t parity) {
   return mbar_wait_bounded_for(bar, parity, kWaitLimitCycles);
 }
 

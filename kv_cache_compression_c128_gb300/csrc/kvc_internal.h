@@ -8,6 +8,8 @@
 #include <cuda.h>  // CUtensorMap (a plain struct; no driver call is linked)
 #include <cuda_runtime.h>
 
+#include "../../include/kvc.h"  // kvc_status
+
 namespace kvc {
 
 // Constants of the section "Gather and Scatter" of the KernelGen Challenge 8
@@ -91,6 +93,8 @@ struct Params {
   int32_t* part_status;           // [2 * max_ctas]
   int32_t* counters;              // [num_outputs]
   uint32_t* error;                // device error word (first error code wins)
+  long long wait_limit;           // SM cycles a pipeline wait may take before the kernel
+                                  // records KVC_ERR_TIMEOUT and abandons the call
   int use_maps;                   // rows apart and every layer has a map (cluster route)
   CUtensorMap maps[kMaxMapLayers];  // per layer, when use_maps
 };
@@ -124,5 +128,34 @@ cudaError_t launch_dequantize(const uint8_t* kv, int64_t num_pages, const int64_
 
 // failure-path self-test (kvc_selftest.cu): one bounded wait that runs out
 cudaError_t launch_selftest_wait(long long limit_cycles, uint32_t* err, cudaStream_t stream);
+
+// The kernels' default limit on one wait, in SM clock cycles (~2 s at 2 GHz).
+constexpr long long kDefaultWaitLimitCycles = 4000000000LL;
+
+// Identity of the CUDA context current on the calling thread (0: none).
+// Per-device set-up (function attributes, symbol addresses) belongs to one
+// context and is made again when another one is current.
+unsigned long long context_id();
+
+// A host step the ABI layer runs on the call's stream after every argument
+// check has passed, right before the launch (kvc_static.cu clears its
+// counters this way, so a refused call writes nothing).
+struct PreLaunch {
+  cudaError_t (*fn)(void* ctx, cudaStream_t stream);
+  void* ctx;
+};
+
+// kvc_compress (include/kvc.h) with a PreLaunch step (null: none).
+kvc_status compress_hooked(const void* state_cache, int64_t num_state_blocks,
+                           const int32_t* token_to_req, const int64_t* positions,
+                           int64_t num_tokens, const int64_t* boundary_token_indices,
+                           int64_t num_outputs, const int32_t* block_table, int64_t num_reqs,
+                           int64_t max_blocks_per_req, const float* rms_norm_weight,
+                           const float* cos_sin_cache, int64_t num_positions,
+                           const int64_t* kv_slot_mapping, int64_t slot_mapping_len,
+                           uint8_t* kv_cache, int64_t num_kv_pages, int32_t block_size,
+                           int32_t compress_ratio, float rms_norm_eps, float* y_out,
+                           void* workspace, size_t workspace_bytes, uint32_t flags, void* stream,
+                           const PreLaunch* pre_launch);
 
 }  // namespace kvc

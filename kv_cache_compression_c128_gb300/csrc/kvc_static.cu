@@ -13,9 +13,10 @@
 //
 // The buffer is shared by every call on a device and keeps what the last call
 // left in it.  Its arrival counters are cleared (cudaMemsetAsync on the
-// caller's stream) before each launch; calls that overlap on the GPU would
-// use the same buffer at once and race, so callers must order them (one
-// stream, or events).
+// caller's stream) once every argument check has passed, right before the
+// launch, so a refused call writes nothing; calls that overlap on the GPU
+// would use the same buffer at once and race, so callers must order them
+// (one stream, or events).
 
 #include <cuda_runtime.h>
 
@@ -23,6 +24,7 @@
 #include <mutex>
 
 #include "../../include/kvc.h"
+#include "kvc_internal.h"
 
 namespace {
 
@@ -35,23 +37,43 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mutex;
-void* g_static_ptr[kMaxDevices] = {};
+struct StaticAddress {
+  unsigned long long ctx = 0;  // context the address belongs to (kvc::context_id)
+  void* ptr = nullptr;
+};
+StaticAddress g_static[kMaxDevices];
 
 // Device address of g_static_scratch on the current device.  Host code only
 // sees a host-side stand-in under the array's name; a kernel must be given
-// the address cudaGetSymbolAddress returns.  Looked up once per device.
+// the address cudaGetSymbolAddress returns.  Looked up once per device and
+// context: after cudaDeviceReset the library's module is loaded again in a
+// new context, and the address is looked up again.
 kvc_status static_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_ERR_CUDA;
+  const unsigned long long ctx = kvc::context_id();
   std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (g_static_ptr[dev] == nullptr) {
+  StaticAddress& a = g_static[dev];
+  if (a.ptr == nullptr || ctx == 0 || a.ctx != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr)
       return KVC_ERR_CUDA;
-    g_static_ptr[dev] = ptr;
+    a.ptr = ptr;
+    a.ctx = kvc::context_id();  // the lookup made a context current
   }
-  *out = g_static_ptr[dev];
+  *out = a.ptr;
   return KVC_OK;
+}
+
+// The bytes to clear before a launch: the arrival counters.
+struct ClearRange {
+  unsigned char* at;
+  size_t bytes;
+};
+
+cudaError_t clear_counters(void* ctx, cudaStream_t stream) {
+  const ClearRange* r = static_cast<const ClearRange*>(ctx);
+  return cudaMemsetAsync(r->at, 0, r->bytes, stream);
 }
 
 }  // namespace
@@ -65,23 +87,24 @@ extern "C" kvc_status kvc_compress_static(
     uint8_t* kv_cache, int64_t num_kv_pages, int32_t block_size, int32_t compress_ratio,
     float rms_norm_eps, float* y_out, uint32_t flags, void* stream) {
   void* scratch = nullptr;
+  ClearRange clear{nullptr, 0};
   if (num_outputs > 0) {
-    const kvc_status st = static_scratch(&scratch);
-    if (st != KVC_OK) return st;
     // Workspace layout: partial states first, the arrival counters from
     // offset kvc_workspace_bytes(0) to kvc_workspace_bytes(num_outputs).
     const size_t counters_at = kvc_workspace_bytes(0);
     const size_t need = kvc_workspace_bytes(num_outputs);
     if (counters_at == 0 || need == 0) return KVC_ERR_CUDA;
     if (need > kStaticScratchBytes) return KVC_ERR_SCRATCH_LIMIT;
-    if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + counters_at, 0, need - counters_at,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return KVC_ERR_CUDA;
+    const kvc_status st = static_scratch(&scratch);
+    if (st != KVC_OK) return st;
+    clear = ClearRange{static_cast<unsigned char*>(scratch) + counters_at, need - counters_at};
   }
-  return kvc_compress(state_cache, num_state_blocks, token_to_req, positions, num_tokens,
-                      boundary_token_indices, num_outputs, block_table, num_reqs,
-                      max_blocks_per_req, rms_norm_weight, cos_sin_cache, num_positions,
-                      kv_slot_mapping, slot_mapping_len, kv_cache, num_kv_pages, block_size,
-                      compress_ratio, rms_norm_eps, y_out, scratch,
-                      scratch ? kStaticScratchBytes : 0, flags, stream);
+  const kvc::PreLaunch hook{&clear_counters, &clear};
+  return kvc::compress_hooked(state_cache, num_state_blocks, token_to_req, positions, num_tokens,
+                              boundary_token_indices, num_outputs, block_table, num_reqs,
+                              max_blocks_per_req, rms_norm_weight, cos_sin_cache, num_positions,
+                              kv_slot_mapping, slot_mapping_len, kv_cache, num_kv_pages,
+                              block_size, compress_ratio, rms_norm_eps, y_out, scratch,
+                              scratch ? kStaticScratchBytes : 0, flags, stream,
+                              scratch ? &hook : nullptr);
 }

@@ -77,7 +77,7 @@ __device__ void producer(const Params& p, StreamKShared& sh, uint8_t* ring, int6
       if (lane == 0) {
         if (*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
           stop = true;
-        } else if (!mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u)) {
+        } else if (!mbar_wait_bounded(&sh.empty_bar[stage], phase ^ 1u, p.wait_limit)) {
           record_error(p.error, kErrTimeout);
           *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;
           stop = true;
@@ -110,7 +110,7 @@ __device__ void producer(const Params& p, StreamKShared& sh, uint8_t* ring, int6
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s)
       if ((issued >> s) & 1u)
-        if (!mbar_wait_bounded(&sh.full_bar[s], (last_parity >> s) & 1u))
+        if (!mbar_wait_drain(&sh.full_bar[s], (last_parity >> s) & 1u))
           record_error(p.error, kErrTimeout);
   }
 }
@@ -209,7 +209,7 @@ __device__ void consumer(const Params& p, StreamKShared& sh, const uint8_t* ring
   for (int64_t u = u0; u < u1; ++u) {
     bool ready = false;
     if (!*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
-      ready = mbar_wait_bounded(&sh.full_bar[stage], phase);
+      ready = mbar_wait_bounded(&sh.full_bar[stage], phase, p.wait_limit);
       if (!ready) {
         record_error(p.error, kErrTimeout);
         *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;

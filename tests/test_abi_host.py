@@ -238,3 +238,10 @@ def test_torch_wrapper_rejects_strided_columns(kvc):
 def test_selftest_wait_rejects_bad_limits(kvc):
     assert kvc.kvc_selftest_wait_timeout(0) == 1
     assert kvc.kvc_selftest_wait_timeout(4_000_000_001) == 1
+
+
+def test_selftest_wait_limit_range(kvc):
+    # host-side range check only (no launch): 0 restores the default
+    assert kvc.kvc_selftest_set_wait_limit(4_000_000_001) == 1
+    assert kvc.kvc_selftest_set_wait_limit(500) == 0
+    assert kvc.kvc_selftest_set_wait_limit(0) == 0

@@ -80,7 +80,39 @@ def test_static_entry_matches_workspace_entry_on_two_calls(kvc, R, T, C, route):
         assert np.array_equal(d["kv_cache"].cpu().numpy(), kv_ref), f"call {call}: kv bytes"
 
 
+def _other_compute_processes():
+    """PIDs of other processes holding a context on this GPU (None: unknown)."""
+    import os
+    import subprocess
+
+    try:
+        uuid = str(torch.cuda.get_device_properties(0).uuid)
+        out = subprocess.run(["nvidia-smi", "--query-compute-apps=gpu_uuid,pid",
+                              "--format=csv,noheader"], capture_output=True, text=True,
+                             timeout=30).stdout
+    except (OSError, subprocess.SubprocessError, AttributeError):
+        return None
+    pids = set()
+    for line in out.splitlines():
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) == 2 and uuid.replace("GPU-", "") in parts[0] and parts[1].isdigit():
+            pids.add(int(parts[1]))
+    return pids - {os.getpid()}
+
+
+def _free_bytes(reads=3):
+    """Device free memory, the largest of a few readings after a sync."""
+    torch.cuda.synchronize()
+    return max(torch.cuda.mem_get_info()[0] for _ in range(reads))
+
+
 def test_static_entry_takes_no_device_memory_per_call(kvc):
+    # Free device memory is a device-wide figure: the comparison assumes that
+    # this process is alone on the GPU, and is skipped when nvidia-smi shows
+    # another process holding a context there.
+    others = _other_compute_processes()
+    if others:
+        pytest.skip(f"other processes on this GPU ({sorted(others)}): free memory is not ours alone")
     case = inputs.make_case(4, 32768, 256, seed=inputs.BASE_SEED + 4343)
     sp = torch.cuda.current_stream().cuda_stream
     d = to_device(case)
@@ -88,13 +120,11 @@ def test_static_entry_takes_no_device_memory_per_call(kvc):
     args = _raw_args(d, case, y, sp)
     flags = kvc.make_flags("streamk")
     assert kvc.kvc_compress_static(*args, flags, sp) == kvc.KVC_OK   # first call: set-up
-    torch.cuda.synchronize()
-    free0, _ = torch.cuda.mem_get_info()
-    for _ in range(3):
+    free0 = _free_bytes()
+    for _ in range(5):
         assert kvc.kvc_compress_static(*args, flags, sp) == kvc.KVC_OK
-    torch.cuda.synchronize()
-    free1, _ = torch.cuda.mem_get_info()
-    assert free1 == free0
+    free1 = _free_bytes()
+    assert free1 >= free0
     assert kvc.kvc_get_device_error(sp) == 0
 
 
