@@ -166,3 +166,121 @@ def test_call_reads_its_positions_from_the_previous_calls_slots(kvc, route):
         assert kvc.kvc_get_device_error(stream) == 0
         assert torch.equal(kv_chain, kv_sync)
         assert torch.equal(y_chain.view(torch.int32), y_sync.view(torch.int32))
+
+
+def _coded_case_a(kvc):
+    """Call A of the index tests: 512 windows whose c is a 0/1 pattern (ones at
+    dims 0 mod 8 below 448), so every 8-byte word of a slot's code region, and
+    every other 4-byte word, reads back as the same code q (checked)."""
+    a = inputs.make_case(8, 65536, 128, seed=inputs.BASE_SEED + 7100)
+    cols = np.arange(512)
+    a.state_bits[:, :, :512] = np.where((cols % 8 == 0) & (cols < 448), 0x3F80, 0).astype(np.uint16)
+    a.rms_norm_weight[:] = 1.0
+    a_state, a_args = _dev(a)
+
+    def run_a():
+        kvc.c128_256_512_compress(a_state, block_size=8, compress_ratio=128, **a_args)
+
+    return a, a_args["kv_cache"], run_a
+
+
+def _chain_b_against_sync(kvc, run_a, run_b, out_b, index_buf, stale_value):
+    """A then B back to back must equal B after a host sync, and differ from
+    B on stale index contents (index_buf filled with stale_value)."""
+    stream = torch.cuda.current_stream().cuda_stream
+    run_a()
+    torch.cuda.synchronize()
+    kv_sync, y_sync = run_b(*out_b())
+    torch.cuda.synchronize()
+    assert kvc.kvc_get_device_error(stream) == 0
+    for _ in range(3):
+        index_buf.fill_(stale_value)
+        kv_stale, _ = run_b(*out_b())
+        torch.cuda.synchronize()
+        assert kvc.kvc_get_device_error(stream) == 0
+        assert not torch.equal(kv_stale, kv_sync)
+        outs = out_b()
+        run_a()
+        kv_chain, y_chain = run_b(*outs)                   # queued right behind A
+        torch.cuda.synchronize()
+        assert kvc.kvc_get_device_error(stream) == 0
+        assert torch.equal(kv_chain, kv_sync)
+        assert torch.equal(y_chain.view(torch.int32), y_sync.view(torch.int32))
+
+
+@pytest.mark.parametrize("route", ["auto", "s2"])
+def test_call_reads_its_requests_from_the_previous_calls_slots(kvc, route):
+    # B's token_to_req IS A's kv_cache read as int32: the request of each of
+    # B's boundary tokens is a code A writes.  A guess of B's index chain made
+    # before the grid dependency wait may hold a stale request; B must still
+    # produce what it produces after A is done.
+    a, a_kv, run_a = _coded_case_a(kvc)
+    words = a_kv.view(-1).view(torch.int32)
+    rng = np.random.Generator(np.random.PCG64(inputs.BASE_SEED + 7201))
+    slots = rng.choice(a.num_outputs, size=256, replace=True)
+    j = rng.integers(0, 56, size=256)
+    bti = np.unique((slots // 64) * 9344 + (slots % 64) * 144 + 2 * j)   # code words of A's slots
+    n_b, t_b, R = bti.size, words.numel(), 128
+    blocks = 256
+    b_state = torch.from_numpy(
+        inputs.make_case(1, 8 * blocks, 16, seed=inputs.BASE_SEED + 7202).state_bits.view(np.int16)
+    ).view(torch.bfloat16).cuda()
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    b_args = dict(token_to_req=words, positions=torch.full((t_b,), 15, dtype=torch.int64, device="cuda"),
+                  boundary_token_indices=t(bti.astype(np.int64)),
+                  block_table=t(rng.integers(0, blocks, size=(R, 2)).astype(np.int32)),
+                  rms_norm_weight=t(a.rms_norm_weight), cos_sin_cache=t(inputs._cos_sin_table(16)),
+                  kv_slot_mapping=t(rng.permutation(n_b).astype(np.int64)))
+    flags = 0 if route == "auto" else kvc.make_flags("cluster", 0, 2)
+
+    def out_b():
+        return (torch.zeros(((n_b + 63) // 64, inputs.KV_PAGE_BYTES), dtype=torch.uint8, device="cuda"),
+                torch.zeros((n_b, 512), dtype=torch.float32, device="cuda"))
+
+    def run_b(kv, yb):
+        kvc.c128_256_512_compress(b_state, block_size=8, compress_ratio=16, y_out=yb,
+                                  flags=flags, kv_cache=kv, **b_args)
+        return kv, yb
+
+    run_a()
+    torch.cuda.synchronize()
+    r = words[torch.from_numpy(bti).cuda()]
+    assert int(r.min()) >= 63 and int(r.max()) < R, "A's code words"
+    _chain_b_against_sync(kvc, run_a, run_b, out_b, words, 40)
+
+
+@pytest.mark.parametrize("route", ["auto", "s2"])
+def test_call_reads_its_boundary_tokens_from_the_previous_calls_slots(kvc, route):
+    # B's boundary_token_indices IS the start of A's kv_cache read as int64:
+    # the 56 code words of A's first slot.  A guess made before the wait may
+    # hold a stale boundary token; B must still match the synchronised run.
+    a, a_kv, run_a = _coded_case_a(kvc)
+    words = a_kv.view(-1).view(torch.int64)
+    n_b = 56
+    bti = words[:n_b]
+    rng = np.random.Generator(np.random.PCG64(inputs.BASE_SEED + 7301))
+    b_state = torch.from_numpy(
+        inputs.make_case(1, 128, 16, seed=inputs.BASE_SEED + 7302).state_bits.view(np.int16)
+    ).view(torch.bfloat16).cuda()
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    b_args = dict(token_to_req=torch.zeros(128, dtype=torch.int32, device="cuda"),
+                  positions=torch.arange(128, dtype=torch.int64, device="cuda"),
+                  boundary_token_indices=bti,
+                  block_table=t(rng.permutation(16).astype(np.int32)[None, :]),
+                  rms_norm_weight=t(a.rms_norm_weight), cos_sin_cache=t(inputs._cos_sin_table(128)),
+                  kv_slot_mapping=t(rng.permutation(n_b).astype(np.int64)))
+    flags = 0 if route == "auto" else kvc.make_flags("cluster", 0, 2)
+
+    def out_b():
+        return (torch.zeros((1, inputs.KV_PAGE_BYTES), dtype=torch.uint8, device="cuda"),
+                torch.zeros((n_b, 512), dtype=torch.float32, device="cuda"))
+
+    def run_b(kv, yb):
+        kvc.c128_256_512_compress(b_state, block_size=8, compress_ratio=16, y_out=yb,
+                                  flags=flags, kv_cache=kv, **b_args)
+        return kv, yb
+
+    run_a()
+    torch.cuda.synchronize()
+    assert int(bti.min()) >= 63 and int(bti.max()) < 128, "A's code words"
+    _chain_b_against_sync(kvc, run_a, run_b, out_b, bti, 40)
