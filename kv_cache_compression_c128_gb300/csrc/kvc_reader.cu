@@ -9,9 +9,10 @@
 //
 // Small calls: one slot per 128 threads, 4 dims per thread: a thread reads 4
 // int8 codes (or 4 bf16 RoPE values) and the group's scale byte, scales
-// exactly with ldexpf and writes one 16-byte (fp32) or 8-byte (bf16) vector.
+// exactly (see "exact decode") and writes one 16-byte (fp32) or 8-byte
+// (bf16) vector.
 // Large calls (more slot pairs than fit on the device at once): one warp per
-// slot on a persistent grid, 8 (fp32 output) or 2 (bf16) slots per warp in
+// slot on a persistent grid, 4 (fp32 output) or 2 (bf16) slots per warp in
 // flight, every load and store coalesced.  584 bytes read and 1 or 2 KiB written per slot.
 
 #include <cuda_bf16.h>
@@ -30,17 +31,58 @@ constexpr int kThreadsPerSlot = kHeadDim / 4;   // 128
 constexpr int kSlotsPerCta = kReaderThreads / kThreadsPerSlot;
 constexpr uint32_t kErrBadIndexReader = 4;
 
+// ---- exact decode -----------------------------------------------------------
+//
+// A stored value is q * 2^e for an int8 code q (any of its 256 byte values)
+// and e = b - 127 for a scale byte b (any of its 256 values).  The product
+// has at most 8 significant bits, so it is exact in fp32 -- and in bf16 --
+// unless |q| 2^e reaches 2^128, where correct rounding gives +-inf; zero
+// codes give +0.  It is formed from exact pieces with no conversion
+// instruction and no library scaling call:
+//   q       = float(2^23 + (q + 128)) - (2^23 + 128): the byte (q + 128) is
+//             placed in the mantissa of 2^23 (integer bit operations), and
+//             the subtraction of two integers below 2^24 is exact;
+//   2^(e-1) = the fp32 with those bits: exponent field b - 1 for b >= 2,
+//             the subnormals 2^-127 (b = 1) and 2^-128 (b = 0);
+//   q 2^e   = (q * 2^(e-1)) * 2: both products are exact or overflow, and
+//             b = 255 (e = 128, whose 2^e is not an fp32 value) needs no
+//             special case: a zero code stays +0, any other overflows.
+// The fp32 result's low 16 bits are zero (at most 8 significant bits, and
+// subnormal results keep their bits at or above 2^-128), so its bf16 form
+// is exactly its high half.
+
+// 2^(e - 1) for the scale byte b = e + 127.
+__device__ __forceinline__ float half_scale(uint32_t b) {
+  return __uint_as_float(b >= 2u ? (b - 1u) << 23 : 0x00200000u << b);
+}
+
+// The four codes of `word` (little-endian int8) times 2^e, hs = half_scale.
+__device__ __forceinline__ void decode4(uint32_t word, float hs, float v[4]) {
+  const uint32_t x = word ^ 0x80808080u;  // q + 128 in every byte
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    // bytes (q + 128, 0, 0, 0x4B): 2^23 + q + 128
+    const float q = __uint_as_float(__byte_perm(x, 0x4B00u, 0x5440u | i)) - 8388736.0f;
+    v[i] = (q * hs) * 2.0f;
+  }
+}
+
+// Two decoded values (each exactly a bf16) as one word of bf16 bits.
+__device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632u);
+}
+
 // What one thread reads for its 4 dims of one slot.
 struct Piece {
   uint32_t codes;  // 4 int8 codes (NOPE dims)
   uint2 raw;       // 4 bf16 words (RoPE dims)
-  int e;           // the group's exponent
+  uint32_t b;      // the group's scale byte
   bool ok;         // the slot is read (non-negative and on a page)
 };
 
 __device__ __forceinline__ Piece load_piece(const uint8_t* __restrict__ kv, int64_t num_pages,
                                             int64_t slot, int d0, int t, uint32_t* err) {
-  Piece pc{0u, make_uint2(0u, 0u), 0, false};
+  Piece pc{0u, make_uint2(0u, 0u), 0u, false};
   if (slot < 0) return pc;
   const int64_t page = slot / kSlotsPerPage, off = slot % kSlotsPerPage;
   if (page >= num_pages) {
@@ -51,7 +93,7 @@ __device__ __forceinline__ Piece load_piece(const uint8_t* __restrict__ kv, int6
   const uint8_t* payload = pg + off * kTokenStride;
   if (d0 < kNopeDim) {
     pc.codes = __ldg(reinterpret_cast<const uint32_t*>(payload + d0));
-    pc.e = static_cast<int>(__ldg(pg + kScaleBase + off * kScaleDim + d0 / kGroup)) - 127;
+    pc.b = __ldg(pg + kScaleBase + off * kScaleDim + d0 / kGroup);
   } else {
     pc.raw = __ldg(reinterpret_cast<const uint2*>(payload + kNopeDim + 2 * (d0 - kNopeDim)));
   }
@@ -64,9 +106,7 @@ __device__ __forceinline__ void store_piece(const Piece& pc, int d0, int t, int6
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   const bool rope = pc.ok && d0 >= kNopeDim;  // RoPE dims: the stored bf16 words, copied as they are
   if (pc.ok && !rope) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      v[i] = ldexpf(static_cast<float>(static_cast<int8_t>((pc.codes >> (8 * i)) & 0xFFu)), pc.e);
+    decode4(pc.codes, half_scale(pc.b), v);
   } else if (rope) {
     v[0] = __uint_as_float(pc.raw.x << 16);
     v[1] = __uint_as_float(pc.raw.x & 0xFFFF0000u);
@@ -76,12 +116,8 @@ __device__ __forceinline__ void store_piece(const Piece& pc, int d0, int t, int6
   if (out_bf16 && rope) {
     reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * kHeadDim)[t] = pc.raw;
   } else if (out_bf16) {
-    uint2 o;
-    o.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[0]))) |
-          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[1]))) << 16);
-    o.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2]))) |
-          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[3]))) << 16);
-    reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * kHeadDim)[t] = o;
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * kHeadDim)[t] =
+        make_uint2(bf16_pair(v[0], v[1]), bf16_pair(v[2], v[3]));
   } else {
     reinterpret_cast<float4*>(static_cast<float*>(out) + m * kHeadDim)[t] =
         make_float4(v[0], v[1], v[2], v[3]);
@@ -192,10 +228,7 @@ __global__ void __launch_bounds__(kReaderThreads) kvc_dequant_warp_kernel(
         if (ok[u] && !is_rope) {
           const int g = d / kGroup;  // 2k + lane / 16
           const uint32_t sw = g < 4 ? scale[u].x : scale[u].y;
-          const int e = static_cast<int>((sw >> (8 * (g & 3))) & 0xFFu) - 127;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            v[i] = ldexpf(static_cast<float>(static_cast<int8_t>((codes[u][k] >> (8 * i)) & 0xFFu)), e);
+          decode4(codes[u][k], half_scale((sw >> (8 * (g & 3))) & 0xFFu), v);
         } else if (is_rope) {
           v[0] = __uint_as_float(rope[u].x << 16);
           v[1] = __uint_as_float(rope[u].x & 0xFFFF0000u);
@@ -207,10 +240,7 @@ __global__ void __launch_bounds__(kReaderThreads) kvc_dequant_warp_kernel(
           if (is_rope) {  // the stored bf16 words, copied as they are
             o = rope[u];
           } else {
-            o.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[0]))) |
-                  (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[1]))) << 16);
-            o.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2]))) |
-                  (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[3]))) << 16);
+            o = make_uint2(bf16_pair(v[0], v[1]), bf16_pair(v[2], v[3]));
           }
           uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * kHeadDim + d);
           if constexpr (kStream) {
@@ -290,19 +320,17 @@ __global__ void __launch_bounds__(kReaderThreads) kvc_dequant_wide16_kernel(
         if (k == 1 && rope_lane) {  // the stored bf16 words, copied as they are
           o = rope[u];
         } else {
-          uint32_t w[4] = {0u, 0u, 0u, 0u};
+          o = make_uint4(0u, 0u, 0u, 0u);
           if (ok[u]) {
             const int g = d / kGroup;
             const uint32_t sw = g < 4 ? scale[u].x : scale[u].y;
-            const int e = static_cast<int>((sw >> (8 * (g & 3))) & 0xFFu) - 127;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t word = i < 4 ? codes[u][k].x : codes[u][k].y;
-              const float v = ldexpf(static_cast<float>(static_cast<int8_t>((word >> (8 * (i & 3))) & 0xFFu)), e);
-              w[i / 2] |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << (16 * (i & 1));
-            }
+            const float hs = half_scale((sw >> (8 * (g & 3))) & 0xFFu);
+            float v[8];
+            decode4(codes[u][k].x, hs, v);
+            decode4(codes[u][k].y, hs, v + 4);
+            o = make_uint4(bf16_pair(v[0], v[1]), bf16_pair(v[2], v[3]), bf16_pair(v[4], v[5]),
+                           bf16_pair(v[6], v[7]));
           }
-          o = make_uint4(w[0], w[1], w[2], w[3]);
         }
         *reinterpret_cast<uint4*>(out + m * kHeadDim + d) = o;
       }
@@ -314,12 +342,14 @@ __global__ void __launch_bounds__(kReaderThreads) kvc_dequant_wide16_kernel(
 
 namespace {
 
-// Large-call kernels, measured on 262,144 slots (random and page order):
-// fp32 output: 8 slots per warp and pass, streaming stores (122.8 -> 112.7
-//   us; either change alone gained at most 3.5 %; 6 and 12 slots were slower);
-// bf16 output: 2 slots per warp and pass, plain stores (79.2 -> 76.8 us;
-//   streaming stores or more slots made it 4-27 % slower).
-constexpr auto kWarpF32 = &kvc_dequant_warp_kernel<8, true>;
+// Large-call kernels, measured on 262,144 slots in random order, with the
+// exact decode (no conversion instruction, no library scaling call):
+// fp32 output: 4 slots per warp and pass, streaming stores: 111.9 us
+//   (2 / 6 / 8 slots: 118.4 / 119.5 / 137.4 us; plain stores at 4: 113.5;
+//   the earlier ldexpf decode at 8 slots: 112.2);
+// bf16 output (16-byte aligned, wide16): 2 slots per warp and pass, plain
+//   stores: 68.2 us (72.2 with the ldexpf decode and a cvt per value).
+constexpr auto kWarpF32 = &kvc_dequant_warp_kernel<4, true>;
 constexpr auto kWarpBf16 = &kvc_dequant_warp_kernel<2, false>;
 constexpr auto kWide16Bf16 = &kvc_dequant_wide16_kernel<2>;
 
