@@ -90,6 +90,9 @@ CASES = [
     # (name, num_reqs, total_tokens, C, route, cluster size, wait limit in SM cycles)
     ("s1", 4, 32768, 128, "cluster", 1, 200),
     ("s1_limit_2000", 4, 32768, 128, "cluster", 1, 2000),
+    # a call small enough that the resolver issues the ring's first pass itself
+    ("s1_small_call", 1, 8192, 128, "cluster", 1, 200),
+    ("s1_small_call_limit_3000", 1, 8192, 512, "cluster", 1, 3000),
     ("s2", 4, 32768, 256, "cluster", 2, 200),
     ("s4", 4, 32768, 512, "cluster", 4, 500),
     ("s8", 1, 8192, 256, "cluster", 8, 500),
