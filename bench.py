@@ -14,7 +14,7 @@ with CUDA events on the launching stream, between device synchronisations
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--no-sweep] [--no-e2e] [--no-cpu] [--state-layout L]
-                  [--sweep-only]
+                  [--sweep-only [--shape NAME]] [--reader-only]
 """
 from __future__ import annotations
 
@@ -666,19 +666,21 @@ def windows_overlap(case) -> bool:
 
 
 def run_sweep(kvc, inputs, device, peak: float, steps=None, warmup: int = 20,
-              detail: bool = False):
+              detail: bool = False, only: str | None = None):
     """The 12 benchmark shapes, the 3 ragged variants, the general-window
     headline and the headline with block_size 16, each timed like the
     headline (steps: 2000 for the small states, 600 for the large ones,
     unless given).  With `detail`, each shape also gets its per-call
     distribution (100 calls, L2 cold and warm) and one single-threaded
-    oracle pass on the host."""
+    oracle pass on the host.  `only`: time just the shape of that name."""
     out = []
     makers = ([lambda i=i: inputs.bench_case(i) for i in range(12)]
               + [lambda c=c: inputs.ragged_case(c) for c in (128, 256, 512)]
               + [lambda: inputs.general_window_case(128, 16), inputs.block16_case])
     for make in makers:
         cs = make()
+        if only is not None and cs.name != only:
+            continue
         n_steps = steps or (2000 if cs.state_bits.nbytes < 100 * 2 ** 20 else 600)
         tc, _ = time_device(kvc, cs, device, n_steps, warmup)
         b = bytes_for(cs)
@@ -739,6 +741,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep-only", action="store_true",
                     help="time only the shape sweep, --steps launches per shape (for ncu)")
+    ap.add_argument("--shape", default=None,
+                    help="with --sweep-only: time only the sweep shape of this name")
+    ap.add_argument("--reader-only", action="store_true",
+                    help="time only the reader (kvc_dequantize) calls (for ncu)")
     ap.add_argument("--state-layout", choices=sorted(LAYOUTS), default="bf16",
                     help="layout of the timed headline state (default: contiguous bf16)")
     args = ap.parse_args()
@@ -773,7 +779,10 @@ def main():
     if args.sweep_only:
         peak, _ = measured_peaks()
         print(json.dumps({"sweep": run_sweep(kvc, inputs, device, peak, args.steps,
-                                             args.warmup)}))
+                                             args.warmup, only=args.shape)}))
+        return
+    if args.reader_only:
+        print(json.dumps({"reader": time_reader(kvc, inputs.headline_case(), device)}))
         return
     case = inputs.make_case(R, T, C, seed=rank_seed(inputs.BASE_SEED + inputs.BENCH_SHAPES.index(HEADLINE), rank),
                             name="headline")
