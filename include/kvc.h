@@ -378,6 +378,32 @@ kvc_status kvc_selftest_wait_timeout(uint64_t limit_cycles, void* stream);
 kvc_status kvc_selftest_set_wait_limit(uint64_t limit_cycles);
 
 /*
+ * Test hook for the guessed first pass of a call on a state whose rows are
+ * adjacent.  A CTA that is resident while the previous kernel on its stream
+ * still runs reads the index arrays as they stand (they may still change),
+ * issues its first copies from those guesses the moment the grid
+ * dependency wait releases, and then checks every guess against the
+ * indices read after the release.  A failed check throws the copied rows
+ * away and copies the right ones; results never depend on which happened.
+ * on = 1: every guess made by calls launched afterwards in this process, on
+ * any device, names the next physical block instead of the right one, so
+ * every guessed first pass fails its check (given at least 2 physical
+ * blocks) and takes that recovery.  on = 0 restores normal guesses; other
+ * values return KVC_ERR_INVALID_ARG.  Not synchronised with calls in flight
+ * on other host threads.
+ */
+kvc_status kvc_selftest_poison_guesses(int32_t on);
+
+/*
+ * Synchronises `stream`, then reads and clears the number of guessed first
+ * passes whose check failed, counted by the kernels of this library on the
+ * current device since the last read.  Indices that no earlier kernel on
+ * the stream changes always pass, so outside kvc_selftest_poison_guesses
+ * the count stays 0 unless a call reads indices the kernel before it writes.
+ */
+kvc_status kvc_selftest_first_pass_rejections(void* stream, uint64_t* out_count);
+
+/*
  * Synchronises `stream`, then reads and clears the device error code
  * recorded by kernels of this library on the current device (KVC_OK if
  * none).  The code is the first one recorded since the last clear.

@@ -164,6 +164,10 @@ def lib():
             L.kvc_selftest_wait_timeout.restype = ctypes.c_int
             L.kvc_selftest_set_wait_limit.argtypes = [ctypes.c_uint64]
             L.kvc_selftest_set_wait_limit.restype = ctypes.c_int
+            L.kvc_selftest_poison_guesses.argtypes = [I32]
+            L.kvc_selftest_poison_guesses.restype = ctypes.c_int
+            L.kvc_selftest_first_pass_rejections.argtypes = [P, P]
+            L.kvc_selftest_first_pass_rejections.restype = ctypes.c_int
             L.kvc_get_device_error.argtypes = [P, P]
             L.kvc_get_device_error.restype = ctypes.c_int
             L.kvc_error_string.argtypes = [ctypes.c_int]
@@ -222,6 +226,23 @@ def kvc_selftest_set_wait_limit(limit_cycles: int) -> int:
     compressions in this process; 0 restores the default.  Returns the
     status."""
     return int(lib().kvc_selftest_set_wait_limit(int(limit_cycles)))
+
+
+def kvc_selftest_poison_guesses(on: bool) -> int:
+    """Test hook: make every guessed first pass of later calls in this
+    process fail its check (True) or guess normally (False).  Returns the
+    status."""
+    return int(lib().kvc_selftest_poison_guesses(1 if on else 0))
+
+
+def kvc_selftest_first_pass_rejections(stream: Optional[int] = None) -> int:
+    """Synchronise `stream`, read and clear the count of guessed first passes
+    that failed their check on the current device."""
+    n = ctypes.c_uint64()
+    st = lib().kvc_selftest_first_pass_rejections(ctypes.c_void_p(stream or 0), ctypes.byref(n))
+    if st != KVC_OK:
+        raise KvcError(st, "kvc_selftest_first_pass_rejections")
+    return int(n.value)
 
 
 def kvc_get_device_error(stream: Optional[int] = None) -> int:

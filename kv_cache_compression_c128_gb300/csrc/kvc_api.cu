@@ -20,6 +20,10 @@ namespace {
 // unless kvc_selftest_set_wait_limit shortened it.
 std::atomic<long long> g_wait_limit{kvc::kDefaultWaitLimitCycles};
 
+// Whether calls launched from now on poison their guessed first passes
+// (kvc_selftest_poison_guesses).
+std::atomic<int> g_poison_guesses{0};
+
 // A driver entry point looked up through the runtime (no link against the
 // driver library); null when the driver does not offer it.
 template <typename Fn>
@@ -58,6 +62,10 @@ namespace {
 // kvc_get_device_error.  Kernels get its device address in Params::error.
 __device__ uint32_t g_error_word;
 
+// Guessed first passes that failed their check since the last
+// kvc_selftest_first_pass_rejections.  Kernels get it in Params::rejections.
+__device__ unsigned long long g_rejections;
+
 constexpr int kMaxDevices = 64;
 
 constexpr int kClusterSizes[] = {1, 2, 4, 8, 16};
@@ -70,6 +78,7 @@ struct DeviceInfo {
   int streamk_ctas_per_sm = 0;
   int cluster_cap[kNumClusterSizes] = {};  // co-resident clusters per size
   uint32_t* error_word = nullptr;
+  unsigned long long* rejections = nullptr;
 };
 
 std::mutex g_mutex;
@@ -104,9 +113,12 @@ kvc_status device_info(DeviceInfo* out) {
     for (int i = 0; i < kNumClusterSizes; ++i) d.cluster_cap[i] = kvc::cluster_capacity(kClusterSizes[i]);
     void* err = nullptr;
     if (cudaGetSymbolAddress(&err, g_error_word) != cudaSuccess || err == nullptr) return KVC_ERR_CUDA;
+    void* rej = nullptr;
+    if (cudaGetSymbolAddress(&rej, g_rejections) != cudaSuccess || rej == nullptr) return KVC_ERR_CUDA;
     d.sms = sms;
     d.streamk_ctas_per_sm = per_sm;
     d.error_word = static_cast<uint32_t*>(err);
+    d.rejections = static_cast<unsigned long long*>(rej);
     d.ctx = kvc::context_id();  // the set-up's runtime calls made a context current
     d.ready = true;
   }
@@ -352,6 +364,8 @@ kvc_status compress_layers(int32_t L, const void* const* state_caches, const Sta
   p.counters = reinterpret_cast<int32_t*>(ws + WL.counters);
   p.error = d.error_word;
   p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  p.rejections = d.rejections;
+  p.poison_guesses = g_poison_guesses.load(std::memory_order_relaxed);
 
   const bool streamk_ok = lay.dtype == KVC_DTYPE_BF16 && p.rows_contiguous &&
                           block_size == kvc::kBlockRows && compress_ratio % kvc::kBlockRows == 0;
@@ -529,6 +543,26 @@ kvc_status kvc_selftest_set_wait_limit(uint64_t limit_cycles) {
   g_wait_limit.store(limit_cycles == 0 ? kvc::kDefaultWaitLimitCycles
                                        : static_cast<long long>(limit_cycles),
                      std::memory_order_relaxed);
+  return KVC_OK;
+}
+
+kvc_status kvc_selftest_poison_guesses(int32_t on) {
+  if (on != 0 && on != 1) return KVC_ERR_INVALID_ARG;
+  g_poison_guesses.store(on, std::memory_order_relaxed);
+  return KVC_OK;
+}
+
+kvc_status kvc_selftest_first_pass_rejections(void* stream, uint64_t* out_count) {
+  if (out_count == nullptr) return KVC_ERR_INVALID_ARG;
+  DeviceInfo d;
+  const kvc_status st = device_info(&d);
+  if (st != KVC_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+  unsigned long long n = 0;
+  if (cudaMemcpy(&n, d.rejections, sizeof n, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  if (n != 0 && cudaMemset(d.rejections, 0, sizeof n) != cudaSuccess) return KVC_ERR_CUDA;
+  *out_count = n;
   return KVC_OK;
 }
 

@@ -30,7 +30,11 @@
 //           32 KiB stages (two bf16 chunks or one fp32 chunk each), each
 //           stage guarded by a full/empty mbarrier pair.  When the rows of a
 //           block are not adjacent: one TMA tensor copy per chunk through a
-//           per-layer tensor map, or one bulk copy per row without one;
+//           per-layer tensor map, or one bulk copy per row without one.
+//           With adjacent rows the ring's first pass goes out from the
+//           resolver, or, when the CTA is resident before the grid
+//           dependency wait releases, from the whole issuer warp, on indices
+//           read early and checked after the release;
 //   warps 0-7 consumers: thread t owns dims 2t, 2t+1 and folds every staged
 //           chunk into its (max, denominator, numerator), a stage of two
 //           full bf16 chunks as 16 rows with one rescale.  Before the grid
@@ -125,6 +129,8 @@ struct ClusterShared {
   FinalScratch fs;
   uint32_t stage_rows[kStages];  // valid rows of each chunk of a stage, 8 bits each (0: unresolved)
   int abort_flag;
+  int first_pass_owner;       // who issues the ring's first pass: 0 not yet, 1 issuer, 2 resolver
+  long long resolver_start;   // clock64() when the resolver started (0: not yet)
 };
 
 __device__ __forceinline__ bool aborted(const int* flag) {
@@ -180,6 +186,161 @@ __device__ __noinline__ void pre_issue_first_pass(const Params& p, ClusterShared
   }
 }
 
+// The stage word of a first-pass stage whose guessed rows were wrong: the
+// consumers skip the stage unread (a real word holds at most 8 rows a chunk).
+constexpr uint32_t kJunkStage = 0xFFFFFFFFu;
+
+// The issuer warp claims the ring's first pass only while the resolver has
+// been running for fewer SM clocks than this (about 0.5 us); after that the
+// resolver's own issue, which needs no check, comes first.  Measured in
+// graph replay over the 12 benchmark shapes: 1000 and 1500 did best; 2000
+// left one 64 MiB shape 0.5 % slower than without guesses, 3000 2 %.
+constexpr long long kClaimWindow = 1000;
+
+// The ring's first pass issued from guesses, by the whole issuer warp
+// (adjacent rows only).  A CTA that is resident while the previous grid on
+// the stream still runs would otherwise idle until the grid dependency wait
+// releases, then walk the index chain (boundary index, then request and
+// position, then block-table entry: three dependent loads, 1-1.5 us from L2
+// under load) before its first copy.  Here lane i resolves unit i of the
+// first pass from the index arrays as they stand, before the wait (L2-only
+// loads, every index bounds-checked, nothing recorded), and the copies go
+// out as soon as the wait releases.  One level of loads then checks every
+// guess: the boundary index, request, position, slot and block-table
+// entries, all at addresses the guesses give.  They are issued before the
+// copies, since a load issued behind this SM's bulk copies waits for their
+// data (measured: the check took 0.5-2 us after the release that way, and
+// about 0.3 us this way).
+//   Every guess held: the lanes write the outputs' slot records and the
+//     stage words, and each stage gets its one arrival, as in the resolver's
+//     own issue (pre_issue_first_pass).
+//   Any guess failed: each stage still gets its arrival (the copies in
+//     flight complete it) with the word kJunkStage; the consumers skip those
+//     stages and the issuer copies the first pass again from the resolver's
+//     FIFO, one ring pass later.  The results are the same either way.
+// This warp and the resolver race for the first pass with a compare-and-
+// swap in shared memory, and this warp enters only within kClaimWindow of
+// the resolver's start: a CTA that became resident after the release would
+// finish its guesses too late to gain.  Returns false only when this warp
+// issued the first pass and a guess failed (the same on every lane).
+// Measured in graph replay against the resolver's issue alone: the
+// headline and every 128 and 256 MiB shape 1.8-2.1 % faster, 1 / 8192 at
+// C = 512 8.6 %; the other 16 and 64 MiB shapes -2.3 .. +0.7 %; calls timed
+// alone unchanged (no earlier grid, so no early CTA).
+template <int S, bool F32>
+__device__ __noinline__ bool guessed_first_pass(const Params& p, ClusterShared<S>& sh, uint8_t* ring,
+                                                int64_t n0, int64_t units, int k_lo, int kj) {
+  using T = StateTraits<F32>;
+  constexpr int CPS = T::kChunksPerStage;
+  const int lane = threadIdx.x & 31;
+  // this warp's part in letting the next grid start launching (the CTA's
+  // other threads give theirs after the wait)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int n_pre = first_pass_stages<F32>(units, kj);
+  const int pre_units = first_pass_units<F32>(n_pre, kj);
+  const bool mine = lane < pre_units;
+  const int piece = lane / kj, kk = lane - piece * kj;
+  const int64_t o = n0 + piece;  // output of the L * N space
+  const int layer = static_cast<int>(o / p.num_outputs);
+  const int64_t n = o - static_cast<int64_t>(layer) * p.num_outputs;
+  const int64_t C = p.compress_ratio, B = p.block_size;
+  const int64_t first_rel = static_cast<int64_t>(kBlockRows) * (k_lo + kk) - C + 1;  // + pos
+  // the guess: the chain of resolve_chunk on the indices as they stand
+  int64_t b = -1, r = -1, pos = -1, l1 = 0, g1 = -1, g2 = 0;
+  int n1 = 0, n2 = 0;
+  bool valid = false;
+  if (mine) {
+    b = ld_index<true>(p.bti + n);
+    if (b >= 0 && b < p.num_tokens) {
+      r = ld_index<true>(p.token_to_req + b);
+      pos = ld_index<true>(p.positions + b);
+      const int64_t left = C - static_cast<int64_t>(kBlockRows) * (k_lo + kk);
+      if (r >= 0 && r < p.num_reqs && pos - C + 1 >= 0) {
+        const int64_t first = pos + first_rel;
+        const int nr = static_cast<int>(left < kBlockRows ? left : kBlockRows);
+        l1 = first / B;
+        const int64_t o1 = first - l1 * B;
+        n1 = static_cast<int>(B - o1 < nr ? B - o1 : nr);
+        n2 = nr - n1;
+        if (l1 + (n2 > 0 ? 1 : 0) < p.max_blocks) {
+          const int32_t* row = p.block_table + r * p.bt_row_stride;
+          g1 = ld_index<true>(row + l1 * p.bt_col_stride);
+          g2 = n2 > 0 ? ld_index<true>(row + (l1 + 1) * p.bt_col_stride) : 0;
+          valid = g1 >= 0 && g1 < p.num_blocks && g2 >= 0 && g2 < p.num_blocks;
+          if (valid && p.poison_guesses) g1 = g1 + 1 < p.num_blocks ? g1 + 1 : 0;
+        }
+      }
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int won = 0;
+  if (lane == 0) {
+    const long long started = *reinterpret_cast<volatile long long*>(&sh.resolver_start);
+    if (started == 0 || clock64() - started < kClaimWindow)
+      won = atomicCAS(&sh.first_pass_owner, 0, 1) == 0;
+  }
+  if (!__shfl_sync(0xffffffffu, won, 0)) return true;  // the resolver issues it
+  // the check's loads, ahead of the copies
+  int64_t b2 = -1, r2 = -1, pos2 = -1, h1 = -1, h2 = 0, slot = -1;
+  if (valid) {
+    const int32_t* row = p.block_table + r * p.bt_row_stride;
+    b2 = ld_index<true>(p.bti + n);
+    r2 = ld_index<true>(p.token_to_req + b);
+    pos2 = ld_index<true>(p.positions + b);
+    h1 = ld_index<true>(row + l1 * p.bt_col_stride);
+    if (n2 > 0) h2 = ld_index<true>(row + (l1 + 1) * p.bt_col_stride);
+    if (kk == 0) slot = ld_index<true>(p.slot_map + (p.slot_by_token ? b : n));
+  }
+  // the copies of the guessed rows (the protocol of pre_issue_first_pass)
+  const int g = piece * ((kj + CPS - 1) / CPS) + kk / CPS;  // stage of the pass
+  const int half = kk % CPS;
+  const int nr = n1 + n2;
+  if (valid) mbar_expect_tx(&sh.full_bar[g], static_cast<uint32_t>(nr * T::kRowBytes));
+  __syncwarp();  // every byte count is announced before any copy is issued
+  if (valid) {
+    const uint64_t policy = evict_first_policy();
+    uint8_t* dst = ring + static_cast<size_t>(g) * T::kStageBytes +
+                   static_cast<size_t>(half) * T::kChunkBytes;
+    const uint8_t* state = p.states[layer];
+    const int64_t o1 = pos + first_rel - l1 * B;
+    bulk_copy_g2s(dst, state + g1 * p.state_block_bytes + o1 * p.state_row_bytes,
+                  n1 * T::kRowBytes, &sh.full_bar[g], policy);
+    if (n2 > 0)
+      bulk_copy_g2s(dst + n1 * T::kRowBytes, state + g2 * p.state_block_bytes, n2 * T::kRowBytes,
+                    &sh.full_bar[g], policy);
+  }
+  // the check: with the same boundary index, request and position the chunk
+  // has the same runs, so equal block-table entries mean equal rows; the
+  // output's slot record passes resolve_chunk's bounds checks
+  bool match = !mine;
+  int64_t pc = -1;
+  if (valid) {
+    match = b2 == b && r2 == r && pos2 == pos && h1 == g1 && h2 == g2;
+    if (kk == 0) {
+      pc = (pos / C) * C;
+      match = match && pc < p.num_positions && (slot < 0 || slot / kSlotsPerPage < p.num_pages);
+    }
+  }
+  const bool ok = __all_sync(0xffffffffu, match);
+  if (ok && mine && kk == 0) {
+    MetaRec& m = sh.meta[piece % kMetaRing];
+    m.slot = slot;
+    m.pc = pc;
+  }
+  // rows of each chunk of the stage, 8 bits per chunk (the closing lane's
+  // word takes its predecessor's chunk when the stage holds two)
+  const uint32_t rows = static_cast<uint32_t>(nr) << (8 * half);
+  const uint32_t prev = __shfl_up_sync(0xffffffffu, rows, 1);
+  const bool closes = mine && (half == CPS - 1 || kk == kj - 1);
+  __syncwarp();  // the slot records are written before any stage's arrival
+  if (closes) {
+    sh.stage_rows[g] = ok ? (rows | (half == 1 ? prev : 0u)) : kJunkStage;
+    mbar_arrive(&sh.full_bar[g]);
+  }
+  if (!ok && lane == 0) atomicAdd(p.rejections, 1ull);
+  return ok;
+}
+
 // kBlocks: also pass each chunk's block and first row (tensor copies need
 // them; adjacent rows leave the two fields alone).
 //
@@ -194,15 +355,19 @@ __device__ __noinline__ void pre_issue_first_pass(const Params& p, ClusterShared
 // the stage barrier first (expect_tx, no arrival), then, after the warp has
 // synchronised, issues its copies, and the lane holding a stage's last chunk
 // writes the stage's row counts and makes the stage's one arrival.  The
-// pre-issue is unconditional (even after an abort), because the issuer
-// counts those stages as issued and its final drain waits for them.  The
 // entries still go through the FIFO, where the issuer only keeps count.
+// A CTA resident before the release may have issued the first pass from
+// guesses already (guessed_first_pass): the resolver issues it only if it
+// wins the claim, which it makes whatever happens (even after an abort),
+// because the issuer counts those stages as issued and its final drain
+// waits for them.
 template <int S, bool F32, bool kBlocks>
 __device__ void resolver(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int64_t n0,
                          int64_t units, int k_lo, int kj) {
   using T = StateTraits<F32>;
   const int lane = threadIdx.x & 31;
   const int n_pre = kBlocks ? 0 : first_pass_stages<F32>(units, kj);
+  if (lane == 0) *reinterpret_cast<volatile long long*>(&sh.resolver_start) = clock64();
   for (int64_t c = 0; c * kFifoChunk < units; ++c) {
     const int64_t i = c * kFifoChunk + lane;
     FifoEntry e{-1, -1, -1, -1, 0, 0, 0, 0, 0, 0, 0};
@@ -228,9 +393,13 @@ __device__ void resolver(const Params& p, ClusterShared<S>& sh, uint8_t* ring, i
       e.kk = kk;
       e.piece = static_cast<int>(q);
     }
-    if (c == 0 && n_pre > 0)
-      pre_issue_first_pass<S, F32>(p, sh, ring, e.off1, e.off2, e.n1, e.n2, e.kk, e.piece, e.layer,
-                                   e.slot, e.pc, i < units, kj, n_pre);
+    if (c == 0 && n_pre > 0) {
+      int won = 0;
+      if (lane == 0) won = atomicCAS(&sh.first_pass_owner, 0, 2) == 0;
+      if (__shfl_sync(0xffffffffu, won, 0))
+        pre_issue_first_pass<S, F32>(p, sh, ring, e.off1, e.off2, e.n1, e.n2, e.kk, e.piece,
+                                     e.layer, e.slot, e.pc, i < units, kj, n_pre);
+    }
     const int h = static_cast<int>(c & 1);
     const uint32_t ph = static_cast<uint32_t>((c >> 1) & 1);
     bool ok = true;
@@ -267,16 +436,19 @@ enum class Copy { kRuns, kTensor, kRows };
 // once).  kRows: the whole warp walks it (lane 0 waits, announces bytes and
 // arrives; the walk costs about 2.5 % against lane 0 alone).
 template <int S, bool F32, Copy kCopy>
-__device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int64_t units, int kj) {
+__device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int64_t units, int kj,
+                       bool first_pass_held) {
   using T = StateTraits<F32>;
   constexpr bool kSplitRows = kCopy == Copy::kRows;
   const int lane = threadIdx.x & 31;
   if (!kSplitRows && lane != 0) return;
   const auto lane0_says = [](bool v) { return kSplitRows ? __shfl_sync(0xffffffffu, v, 0) : v; };
   const uint64_t policy = evict_first_policy();
-  // the first pass's stages are issued by the resolver (adjacent rows); they
-  // count as issued at phase 0 from the start, so the drain waits for them
-  // (the issuer starts after their units, at the stage that follows them)
+  // the first pass's stages are issued by the resolver or from guesses
+  // (adjacent rows); they count as issued at phase 0 from the start, so the
+  // drain waits for them.  The issuer starts at the stage that follows them,
+  // with the units after them, or with the first unit again when the
+  // guessed first pass failed its check (first_pass_held false).
   const int n_pre = kCopy == Copy::kRuns ? first_pass_stages<F32>(units, kj) : 0;
   const int pre_units = n_pre > 0 ? first_pass_units<F32>(n_pre, kj) : 0;
   int stage = n_pre == T::kNumStages ? 0 : n_pre;
@@ -298,7 +470,7 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
     }
     if (!lane0_says(ok)) break;
     const int64_t cnt = units - c * kFifoChunk < kFifoChunk ? units - c * kFifoChunk : kFifoChunk;
-    for (int j = c == 0 ? pre_units : 0; j < cnt; ++j) {
+    for (int j = c == 0 && first_pass_held ? pre_units : 0; j < cnt; ++j) {
       const FifoEntry e = sh.fifo[h][j];
       const int half = e.kk % T::kChunksPerStage;  // which chunk of its stage
       const bool closes = half == T::kChunksPerStage - 1 || e.kk == kj - 1;
@@ -434,6 +606,14 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
           set_abort(&sh.abort_flag);
         }
       }
+      const uint32_t word = ready ? sh.stage_rows[stage] : 0u;
+      if (word == kJunkStage) {  // a guessed first-pass stage that failed its check
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty_bar[stage]);
+        if (++stage == T::kNumStages) { stage = 0; phase ^= 1u; }
+        kk -= T::kChunksPerStage;
+        continue;
+      }
       if (kk == 0 && ready) {
         // load what the finalise needs now, so its latency hides behind the window
         if (active) w = __ldg(reinterpret_cast<const float2*>(p.weights[layer] + d0));
@@ -443,7 +623,6 @@ __device__ void consumers(const Params& p, ClusterShared<S>& sh, const uint8_t* 
           sn = __ldg(p.cos_sin + meta.pc * kRopeDim + kRopeDim / 2 + jp);
         }
       }
-      const uint32_t word = ready ? sh.stage_rows[stage] : 0u;
       constexpr uint32_t kTwoFull = kBlockRows | (kBlockRows << 8);
       if (!F32 && T::kChunksPerStage == 2 && kk + 1 < kj && word == kTwoFull) {
         // two full chunks: 16 rows, 2 KiB apart, one shared rescale
@@ -624,6 +803,8 @@ __global__ void __launch_bounds__(kClusterThreads, 2)
     mbar_init(&sh.part_bar, 1);
     mbar_init(&sh.ss_bar, 1);
     sh.abort_flag = 0;
+    sh.first_pass_owner = 0;
+    sh.resolver_start = 0;
     fence_mbar_init();
   }
   // With S > 1 the peers' barriers must exist before the first remote store.
@@ -652,11 +833,18 @@ __global__ void __launch_bounds__(kClusterThreads, 2)
   if (threadIdx.x < 32 && n0 < n1 && kj > 0)
     prefetch_first_stages<F32>(p, n0, (n1 - n0) * kj, k_lo, kj, maps);
   // Wait for the previous grid on the stream (programmatic dependent launch)
-  // before reading any input for a result, and let the next one start launching.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // before reading any input for a result, and let the next one start
+  // launching.  With adjacent rows the issuer warp waits inside
+  // guessed_first_pass.
+  const int warp = threadIdx.x >> 5;
+  bool first_pass_held = true;
+  if (!kApart && warp == kIssuerWarp && p.rows_contiguous && n0 < n1 && kj > 0) {
+    first_pass_held = guessed_first_pass<S, F32>(p, sh, smem, n0, (n1 - n0) * kj, k_lo, kj);
+  } else {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  }
   if (n0 < n1 && kj > 0) {
-    const int warp = threadIdx.x >> 5;
     const int64_t units = (n1 - n0) * kj;
     if (warp == kResolverWarp) {
       resolver<S, F32, kApart>(p, sh, smem, n0, units, k_lo, kj);
@@ -665,12 +853,12 @@ __global__ void __launch_bounds__(kClusterThreads, 2)
         // Rows are adjacent whenever this kernel runs.  The row-copy branch
         // stays in its code all the same: without it the kernel's code layout
         // changed and the 64 MiB C = 128 shape measured 1.5 % slower.
-        if (p.rows_contiguous) issuer<S, F32, Copy::kRuns>(p, sh, smem, units, kj);
-        else issuer<S, F32, Copy::kRows>(p, sh, smem, units, kj);
+        if (p.rows_contiguous) issuer<S, F32, Copy::kRuns>(p, sh, smem, units, kj, first_pass_held);
+        else issuer<S, F32, Copy::kRows>(p, sh, smem, units, kj, true);
       } else if (maps) {
-        issuer<S, F32, Copy::kTensor>(p, sh, smem, units, kj);
+        issuer<S, F32, Copy::kTensor>(p, sh, smem, units, kj, true);
       } else {
-        issuer<S, F32, Copy::kRows>(p, sh, smem, units, kj);
+        issuer<S, F32, Copy::kRows>(p, sh, smem, units, kj, true);
       }
     } else {
       consumers<S, F32>(p, sh, smem, n0, n1, kj, rank, cluster_waited);

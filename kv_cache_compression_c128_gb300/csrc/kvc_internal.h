@@ -95,6 +95,8 @@ struct Params {
   uint32_t* error;                // device error word (first error code wins)
   long long wait_limit;           // SM cycles a pipeline wait may take before the kernel
                                   // records KVC_ERR_TIMEOUT and abandons the call
+  unsigned long long* rejections; // device counter of guessed first passes that failed their check
+  int poison_guesses;             // test hook: guesses name the next physical block
   int use_maps;                   // rows apart and every layer has a map (cluster route)
   CUtensorMap maps[kMaxMapLayers];  // per layer, when use_maps
 };

@@ -245,3 +245,16 @@ def test_selftest_wait_limit_range(kvc):
     assert kvc.kvc_selftest_set_wait_limit(4_000_000_001) == 1
     assert kvc.kvc_selftest_set_wait_limit(500) == 0
     assert kvc.kvc_selftest_set_wait_limit(0) == 0
+
+
+def test_selftest_poison_guesses_range(kvc):
+    # host-side range check only (no launch): 0 restores normal guesses
+    assert kvc.lib().kvc_selftest_poison_guesses(2) == 1
+    assert kvc.lib().kvc_selftest_poison_guesses(-1) == 1
+    assert kvc.kvc_selftest_poison_guesses(True) == 0
+    assert kvc.kvc_selftest_poison_guesses(False) == 0
+
+
+def test_selftest_first_pass_rejections_needs_an_output(kvc):
+    lib = kvc.lib()
+    assert lib.kvc_selftest_first_pass_rejections(None, None) == 1

@@ -1,0 +1,143 @@
+"""GPU: the guessed first pass of a call queued behind another, and its recovery.
+
+A CTA of the cluster kernel that is resident while the previous kernel on
+its stream still runs reads the index arrays before its grid dependency
+wait, issues the ring's first copies from those guesses as soon as the wait
+releases, and then checks every guess against the indices read after the
+release.  A failed check marks the copied stages to be skipped, and the
+issuer copies the right rows one ring pass later.  This only happens to a
+call queued right behind another kernel, so every call here is queued back
+to back with others on one stream, into buffers made before the first is
+queued (a copy or fill between two calls would end the overlap), behind a
+spin kernel that holds the stream until the host has queued them all.
+
+kvc_selftest_poison_guesses makes every guess name the next physical block,
+so every guessed first pass fails its check.  Checked per layout: with the
+poison, the device counts rejected first passes, and every call of the
+chain writes exactly the bytes (and y) of the same call made alone, which
+meets the parity bar against the oracle; without it, no first pass is
+rejected, since nothing changes the indices.
+"""
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_compression_c128_gb300 import inputs
+from kvc_testlib import assert_parity, to_device
+
+pytestmark = pytest.mark.gpu
+
+CHAIN = 6  # calls queued back to back
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import kv_cache_compression_c128_gb300 as kvc
+
+    kvc.build()
+    yield kvc
+    kvc.kvc_selftest_poison_guesses(False)
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+HOLD_CYCLES = 20_000_000  # about 10 ms of spinning: far longer than queueing the calls takes
+
+
+def _calls(kvc, case, d, n, layers=1, flags=0):
+    """n calls of `case` queued back to back, each into its own copies of
+    the prefilled kv_cache (one per layer) and its own y; returns
+    [(kv arrays per layer, y)] after checking the device error word.  With
+    n > 1 the calls wait behind a spin kernel while the host queues them, so
+    that each starts inside the one before it."""
+    N = case.num_outputs
+    kvs = [[d["kv_cache"].clone() for _ in range(layers)] for _ in range(n)]
+    ys = [torch.full((layers * N, 512), float("nan"), dtype=torch.float32, device="cuda")
+          for _ in range(n)]
+    torch.cuda.synchronize()
+    if n > 1:
+        torch.cuda._sleep(HOLD_CYCLES)
+    for kv, y in zip(kvs, ys):
+        if layers == 1:
+            kvc.c128_256_512_compress(block_size=case.block_size,
+                                      compress_ratio=case.compress_ratio,
+                                      rms_norm_eps=case.rms_norm_eps, y_out=y, flags=flags,
+                                      **dict(d, kv_cache=kv[0]))
+        else:
+            kvc.compress_layers([d["state_cache"]] * layers, d["token_to_req"], d["positions"],
+                                d["boundary_token_indices"], d["block_table"],
+                                [d["rms_norm_weight"]] * layers, d["cos_sin_cache"],
+                                d["kv_slot_mapping"], kv, case.block_size, case.compress_ratio,
+                                case.rms_norm_eps, y_out=y, flags=flags)
+    assert kvc.kvc_get_device_error(_stream()) == 0
+    return [([k.cpu().numpy() for k in kv], y.cpu().numpy()) for kv, y in zip(kvs, ys)]
+
+
+def _check_chain(kvc, oracle_mod, case, d, layers=1, flags=0, oracle=True):
+    # the call alone: nothing before it on the stream but the buffer fills
+    kvc.kvc_selftest_first_pass_rejections(_stream())  # clears the count
+    (kv_ref, y_ref), = _calls(kvc, case, d, 1, layers, flags)
+    if oracle:
+        assert_parity(oracle_mod, case, kv_ref[0], y_ref[:case.num_outputs])
+    kvc.kvc_selftest_first_pass_rejections(_stream())
+
+    # without the poison every guess holds
+    for kv, y in _calls(kvc, case, d, CHAIN, layers, flags):
+        assert all(np.array_equal(a, b) for a, b in zip(kv, kv_ref))
+        assert np.array_equal(y.view(np.int32), y_ref.view(np.int32))
+    assert kvc.kvc_selftest_first_pass_rejections(_stream()) == 0
+
+    # with it every guessed first pass is rejected, and the results stand
+    assert kvc.kvc_selftest_poison_guesses(True) == 0
+    try:
+        chain = _calls(kvc, case, d, CHAIN, layers, flags)
+        rejected = kvc.kvc_selftest_first_pass_rejections(_stream())
+    finally:
+        assert kvc.kvc_selftest_poison_guesses(False) == 0
+    assert rejected > 0
+    for kv, y in chain:
+        assert all(np.array_equal(a, b) for a, b in zip(kv, kv_ref))
+        assert np.array_equal(y.view(np.int32), y_ref.view(np.int32))
+    return rejected
+
+
+CASES = [
+    # (name, num_reqs, total_tokens, C, block_size, boundaries per request, cluster size)
+    # 16 outputs on 8-CTA clusters: 128 CTAs, the next call wholly resident early
+    ("r1_c512", 1, 8192, 512, 8, None, 0),
+    # 64 outputs on 4-CTA clusters: the first pass is each CTA's whole window
+    ("r1_c128", 1, 8192, 128, 8, None, 0),
+    # 256 CTAs of one output each: 48 of the next call's CTAs resident early
+    ("r4_c128", 4, 32768, 128, 8, None, 0),
+    ("r4_c256_s2", 4, 32768, 256, 8, None, 2),
+    # windows at any start in blocks of 16 rows: chunks split between blocks
+    ("general_b16", 2, 4096, 100, 16, 24, 0),
+    ("general_b24_s4", 3, 1440, 37, 24, 16, 4),
+]
+
+
+@pytest.mark.parametrize("name,R,T,C,B,nb,S", CASES, ids=[c[0] for c in CASES])
+def test_rejected_guesses_leave_results_alone(kvc, oracle_mod, name, R, T, C, B, nb, S):
+    case = inputs.make_case(R, T, C, seed=inputs.BASE_SEED + 5300 + C + B, block_size=B,
+                            boundaries_per_req=nb, kv_fill=91)
+    flags = kvc.make_flags("cluster", 0, S) if S else 0
+    _check_chain(kvc, oracle_mod, case, to_device(case), flags=flags)
+
+
+def test_rejected_guesses_on_an_fp32_state(kvc, oracle_mod):
+    case = inputs.make_case(2, 8192, 128, seed=inputs.BASE_SEED + 5400, kv_fill=92)
+    d = to_device(case)
+    st32 = inputs.fp32_state(case.num_state_blocks, case.block_size, inputs.BASE_SEED + 5401)
+    d["state_cache"] = torch.from_numpy(st32).cuda()
+    # parity of the fp32 state itself is covered elsewhere; here the chain
+    # must reproduce the call made alone
+    _check_chain(kvc, oracle_mod, case, d, oracle=False)
+
+
+def test_rejected_guesses_in_a_multi_layer_call(kvc, oracle_mod):
+    case = inputs.make_case(1, 8192, 256, seed=inputs.BASE_SEED + 5500, kv_fill=93)
+    _check_chain(kvc, oracle_mod, case, to_device(case), layers=4)
