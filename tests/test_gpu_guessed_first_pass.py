@@ -23,7 +23,7 @@ import pytest
 import torch
 
 from kv_cache_compression_c128_gb300 import inputs
-from kvc_testlib import assert_parity, to_device
+from kvc_testlib import assert_parity, slot_byte_ranges, slots_of_case, to_device, written_mask
 
 pytestmark = pytest.mark.gpu
 
@@ -141,3 +141,65 @@ def test_rejected_guesses_on_an_fp32_state(kvc, oracle_mod):
 def test_rejected_guesses_in_a_multi_layer_call(kvc, oracle_mod):
     case = inputs.make_case(1, 8192, 256, seed=inputs.BASE_SEED + 5500, kv_fill=93)
     _check_chain(kvc, oracle_mod, case, to_device(case), layers=4)
+
+
+KVC_ERR_TIMEOUT = 5
+
+
+@pytest.mark.parametrize("R,T,C,limit", [(1, 8192, 512, 500), (4, 32768, 128, 500)],
+                         ids=["r1_c512", "r4_c128"])
+def test_abort_after_rejected_guesses(kvc, oracle_mod, R, T, C, limit):
+    # both test hooks at once: every guessed first pass fails its check and
+    # the pipeline waits give up early.  The stages copied from the guesses
+    # are counted as issued, so each CTA still waits for them to land before
+    # it exits; every slot must end up whole or untouched.
+    case = inputs.make_case(R, T, C, seed=inputs.BASE_SEED + 5600 + C, kv_fill=94)
+    d = to_device(case)
+    (kv_ref, y_ref), = _calls(kvc, case, d, 1)
+    kv_ref, y_ref = kv_ref[0], y_ref[:case.num_outputs]
+    kvc.kvc_selftest_first_pass_rejections(_stream())
+    assert kvc.kvc_selftest_poison_guesses(True) == 0
+    assert kvc.kvc_selftest_set_wait_limit(limit) == 0
+    try:
+        N = case.num_outputs
+        kvs = [d["kv_cache"].clone() for _ in range(CHAIN)]
+        ys = [torch.full((N, 512), float("nan"), dtype=torch.float32, device="cuda")
+              for _ in range(CHAIN)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(HOLD_CYCLES)
+        for kv, y in zip(kvs, ys):
+            kvc.c128_256_512_compress(block_size=case.block_size,
+                                      compress_ratio=case.compress_ratio,
+                                      rms_norm_eps=case.rms_norm_eps, y_out=y,
+                                      **dict(d, kv_cache=kv))
+        err = kvc.kvc_get_device_error(_stream())  # synchronises: every call returned
+        rejected = kvc.kvc_selftest_first_pass_rejections(_stream())
+    finally:
+        assert kvc.kvc_selftest_set_wait_limit(0) == 0
+        assert kvc.kvc_selftest_poison_guesses(False) == 0
+    assert err == KVC_ERR_TIMEOUT
+    assert rejected > 0
+    slots = slots_of_case(case)
+    inside = written_mask(case.kv_cache.shape, slots).reshape(-1)
+    pre = case.kv_cache.reshape(-1)
+    ref = kv_ref.reshape(-1)
+    abandoned = 0
+    for kv, y in zip(kvs, ys):
+        got, yg = kv.cpu().numpy().reshape(-1), y.cpu().numpy()
+        assert np.array_equal(got[~inside], pre[~inside]), "bytes outside the slots changed"
+        for n, s in enumerate(slots):
+            if s < 0:
+                continue
+            p0, s0 = slot_byte_ranges(s)
+            rng = np.r_[p0:p0 + 576, s0:s0 + 8]
+            if np.array_equal(got[rng], ref[rng]) and not np.array_equal(ref[rng], pre[rng]):
+                assert np.array_equal(yg[n].view(np.int32), y_ref[n].view(np.int32))
+            else:
+                assert np.array_equal(got[rng], pre[rng]), f"output {n}: slot neither whole nor untouched"
+                assert np.all(np.isnan(yg[n]))
+                abandoned += 1
+    assert abandoned >= 1
+    # hooks off: the next chain is whole again
+    for kv, y in _calls(kvc, case, d, 2):
+        assert np.array_equal(kv[0], kv_ref)
+        assert np.array_equal(y.view(np.int32), y_ref.view(np.int32))
