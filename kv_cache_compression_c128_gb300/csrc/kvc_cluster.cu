@@ -209,8 +209,8 @@ constexpr long long kClaimWindow = 1000;
 // guess: the boundary index, request, position, slot and block-table
 // entries, all at addresses the guesses give.  They are issued before the
 // copies, since a load issued behind this SM's bulk copies waits for their
-// data (measured: the check took 0.5-2 us after the release that way, and
-// about 0.3 us this way).
+// data (measured: the check finished 1.8-2.6 us after the release that way,
+// about 1.0 us this way).
 //   Every guess held: the lanes write the outputs' slot records and the
 //     stage words, and each stage gets its one arrival, as in the resolver's
 //     own issue (pre_issue_first_pass).
@@ -224,8 +224,8 @@ constexpr long long kClaimWindow = 1000;
 // finish its guesses too late to gain.  Returns false only when this warp
 // issued the first pass and a guess failed (the same on every lane).
 // Measured in graph replay against the resolver's issue alone: the
-// headline and every 128 and 256 MiB shape 1.8-2.1 % faster, 1 / 8192 at
-// C = 512 8.6 %; the other 16 and 64 MiB shapes -2.3 .. +0.7 %; calls timed
+// headline and every 128 and 256 MiB shape 1.6-1.9 % faster, 1 / 8192 at
+// C = 512 8.5 %; the other 16 and 64 MiB shapes -2.3 .. +0.6 %; calls timed
 // alone unchanged (no earlier grid, so no early CTA).
 template <int S, bool F32>
 __device__ __noinline__ bool guessed_first_pass(const Params& p, ClusterShared<S>& sh, uint8_t* ring,
