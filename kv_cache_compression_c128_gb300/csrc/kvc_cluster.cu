@@ -79,9 +79,10 @@ struct StateTraits {
 };
 
 // Stages of the ring's first pass over a CTA's `units` chunks (kj per
-// output): the resolver issues their copies itself, right after resolving
-// them, instead of handing them to the issuer (adjacent rows only).  A stage
-// holds up to kChunksPerStage consecutive chunks of one output.
+// output): their copies go out from the resolver right after it resolves
+// them, or from the issuer warp on guessed indices (guessed_first_pass),
+// instead of through the FIFO (adjacent rows only).  A stage holds up to
+// kChunksPerStage consecutive chunks of one output.
 template <bool F32>
 __device__ __forceinline__ int first_pass_stages(int64_t units, int kj) {
   using T = StateTraits<F32>;
