@@ -228,7 +228,7 @@ constexpr long long kClaimWindow = 1000;
 // headline and every 128 and 256 MiB shape 1.6-1.9 % faster, 1 / 8192 at
 // C = 512 8.5 %; the other 16 and 64 MiB shapes -2.3 .. +0.6 %; calls timed
 // alone unchanged (no earlier grid, so no early CTA).
-template <int S, bool F32>
+template <int S, bool F32, bool kTensorCopies>
 __device__ __noinline__ bool guessed_first_pass(const Params& p, ClusterShared<S>& sh, uint8_t* ring,
                                                 int64_t n0, int64_t units, int k_lo, int kj) {
   using T = StateTraits<F32>;
@@ -304,11 +304,22 @@ __device__ __noinline__ bool guessed_first_pass(const Params& p, ClusterShared<S
                    static_cast<size_t>(half) * T::kChunkBytes;
     const uint8_t* state = p.states[layer];
     const int64_t o1 = pos + first_rel - l1 * B;
-    bulk_copy_g2s(dst, state + g1 * p.state_block_bytes + o1 * p.state_row_bytes,
-                  n1 * T::kRowBytes, &sh.full_bar[g], policy);
-    if (n2 > 0)
-      bulk_copy_g2s(dst + n1 * T::kRowBytes, state + g2 * p.state_block_bytes, n2 * T::kRowBytes,
-                    &sh.full_bar[g], policy);
+    if constexpr (!kTensorCopies) {
+      bulk_copy_g2s(dst, state + g1 * p.state_block_bytes + o1 * p.state_row_bytes,
+                    n1 * T::kRowBytes, &sh.full_bar[g], policy);
+      if (n2 > 0)
+        bulk_copy_g2s(dst + n1 * T::kRowBytes, state + g2 * p.state_block_bytes, n2 * T::kRowBytes,
+                      &sh.full_bar[g], policy);
+    } else if (n1 == kBlockRows) {  // the chunk's 8 rows in one block: one tensor copy
+      tensor_copy_g2s(dst, &p.maps[layer], static_cast<int>(o1), static_cast<int>(g1),
+                      &sh.full_bar[g], policy);
+    } else {  // split between two blocks: row by row
+      for (int r = 0; r < nr; ++r) {
+        const long long off = r < n1 ? g1 * p.state_block_bytes + (o1 + r) * p.state_row_bytes
+                                     : g2 * p.state_block_bytes + (r - n1) * p.state_row_bytes;
+        bulk_copy_g2s(dst + r * T::kRowBytes, state + off, T::kRowBytes, &sh.full_bar[g], policy);
+      }
+    }
   }
   // the check: with the same boundary index, request and position the chunk
   // has the same runs, so equal block-table entries mean equal rows; the
@@ -446,11 +457,17 @@ __device__ void issuer(const Params& p, ClusterShared<S>& sh, uint8_t* ring, int
   const auto lane0_says = [](bool v) { return kSplitRows ? __shfl_sync(0xffffffffu, v, 0) : v; };
   const uint64_t policy = evict_first_policy();
   // the first pass's stages are issued by the resolver or from guesses
-  // (adjacent rows); they count as issued at phase 0 from the start, so the
-  // drain waits for them.  The issuer starts at the stage that follows them,
-  // with the units after them, or with the first unit again when the
-  // guessed first pass failed its check (first_pass_held false).
-  const int n_pre = kCopy == Copy::kRuns ? first_pass_stages<F32>(units, kj) : 0;
+  // (adjacent rows), or from guesses alone (rows apart through tensor maps);
+  // they count as issued at phase 0 from the start, so the drain waits for
+  // them.  The issuer starts at the stage that follows them, with the units
+  // after them, or with the first unit again when the guessed first pass
+  // failed its check (first_pass_held false).
+  // (rows apart through tensor maps: only when this warp claimed the first
+  // pass, since the resolver never issues it there)
+  const int n_pre = kCopy == Copy::kRuns ||
+                            (kCopy == Copy::kTensor && sh.first_pass_owner == 1)
+                        ? first_pass_stages<F32>(units, kj)
+                        : 0;
   const int pre_units = n_pre > 0 ? first_pass_units<F32>(n_pre, kj) : 0;
   int stage = n_pre == T::kNumStages ? 0 : n_pre;
   uint32_t phase = n_pre == T::kNumStages ? 1u : 0u;
@@ -835,12 +852,14 @@ __global__ void __launch_bounds__(kClusterThreads, 2)
     prefetch_first_stages<F32>(p, n0, (n1 - n0) * kj, k_lo, kj, maps);
   // Wait for the previous grid on the stream (programmatic dependent launch)
   // before reading any input for a result, and let the next one start
-  // launching.  With adjacent rows the issuer warp waits inside
-  // guessed_first_pass.
+  // launching.  With adjacent rows, or rows apart copied through tensor
+  // maps, the issuer warp waits inside guessed_first_pass.
   const int warp = threadIdx.x >> 5;
   bool first_pass_held = true;
   if (!kApart && warp == kIssuerWarp && p.rows_contiguous && n0 < n1 && kj > 0) {
-    first_pass_held = guessed_first_pass<S, F32>(p, sh, smem, n0, (n1 - n0) * kj, k_lo, kj);
+    first_pass_held = guessed_first_pass<S, F32, false>(p, sh, smem, n0, (n1 - n0) * kj, k_lo, kj);
+  } else if (kApart && maps && warp == kIssuerWarp && n0 < n1 && kj > 0) {
+    first_pass_held = guessed_first_pass<S, F32, true>(p, sh, smem, n0, (n1 - n0) * kj, k_lo, kj);
   } else {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -857,7 +876,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2)
         if (p.rows_contiguous) issuer<S, F32, Copy::kRuns>(p, sh, smem, units, kj, first_pass_held);
         else issuer<S, F32, Copy::kRows>(p, sh, smem, units, kj, true);
       } else if (maps) {
-        issuer<S, F32, Copy::kTensor>(p, sh, smem, units, kj, true);
+        issuer<S, F32, Copy::kTensor>(p, sh, smem, units, kj, first_pass_held);
       } else {
         issuer<S, F32, Copy::kRows>(p, sh, smem, units, kj, true);
       }

@@ -203,3 +203,37 @@ def test_abort_after_rejected_guesses(kvc, oracle_mod, R, T, C, limit):
     for kv, y in _calls(kvc, case, d, 2):
         assert np.array_equal(kv[0], kv_ref)
         assert np.array_equal(y.view(np.int32), y_ref.view(np.int32))
+
+
+def _rows_apart(case, state, row_pad):
+    """`state` ([G, B, 1024], bf16 bits or fp32) on the device with each row
+    `row_pad` elements after the previous one's end (NaN in the gaps)."""
+    G, B, W = state.shape
+    rs, bs = W + row_pad, B * (W + row_pad)
+    flat = inputs.embed_strided(state, bs, rs)
+    if flat.dtype == np.float32:
+        dev = torch.from_numpy(flat).cuda()
+    else:
+        dev = torch.from_numpy(flat.view(np.int16)).view(torch.bfloat16).cuda()
+    return dev.as_strided((G, B, W), (bs, rs, 1))
+
+
+@pytest.mark.parametrize("dtype,R,T,C,B,nb", [
+    ("bf16", 2, 8192, 128, 8, None),
+    ("bf16", 1, 8192, 512, 8, None),
+    ("fp32", 2, 8192, 256, 8, None),
+    # windows at any start in blocks of 16 rows: chunks split between two
+    # blocks go row by row, the others by one tensor copy
+    ("bf16", 2, 4096, 100, 16, 24),
+], ids=["bf16_c128", "bf16_c512", "fp32_c256", "bf16_general_b16"])
+def test_rejected_guesses_with_rows_apart(kvc, oracle_mod, dtype, R, T, C, B, nb):
+    # rows 64 elements apart are copied through per-layer TMA tensor maps,
+    # and the guessed first pass there issues tensor copies too
+    case = inputs.make_case(R, T, C, seed=inputs.BASE_SEED + 5700 + C + B, block_size=B,
+                            boundaries_per_req=nb, kv_fill=95)
+    d = to_device(case)
+    st = case.state_bits if dtype == "bf16" else \
+        inputs.fp32_state(case.num_state_blocks, case.block_size, inputs.BASE_SEED + 5701)
+    d["state_cache"] = _rows_apart(case, st, 64)
+    rejected = _check_chain(kvc, oracle_mod, case, d, oracle=dtype == "bf16")
+    assert rejected > 0
