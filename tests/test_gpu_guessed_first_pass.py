@@ -237,3 +237,13 @@ def test_rejected_guesses_with_rows_apart(kvc, oracle_mod, dtype, R, T, C, B, nb
     d["state_cache"] = _rows_apart(case, st, 64)
     rejected = _check_chain(kvc, oracle_mod, case, d, oracle=dtype == "bf16")
     assert rejected > 0
+
+
+def test_rejected_guesses_in_a_multi_layer_call_with_rows_apart(kvc, oracle_mod):
+    # 3 layers whose states share one strided view (rows 64 elements
+    # apart): the per-layer tensor maps and the guessed tensor copies
+    case = inputs.make_case(1, 8192, 256, seed=inputs.BASE_SEED + 5800, kv_fill=96)
+    d = to_device(case)
+    d["state_cache"] = _rows_apart(case, case.state_bits, 64)
+    rejected = _check_chain(kvc, oracle_mod, case, d, layers=3)
+    assert rejected > 0
