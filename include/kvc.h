@@ -25,6 +25,12 @@
  * All pointers name device memory of the current CUDA device unless stated
  * otherwise; the caller owns every buffer.  Calls are asynchronous on the
  * given stream and never synchronise it (kvc_get_device_error excepted).
+ * A call may start while the kernel before it on the stream still runs
+ * (programmatic dependent launch).  It may then read its index arrays,
+ * warm L2 with its first rows and even copy rows those indices name, but
+ * every value that reaches a result is read, or checked against a read,
+ * after that kernel has finished: a call may read what the kernel before
+ * it writes.
  * The library's own per-device set-up (kernel attributes, the addresses of
  * its device-side words) is made at the first call in a CUDA context and made
  * again when another context is current on that device, e.g. after
