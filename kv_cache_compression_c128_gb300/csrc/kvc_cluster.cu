@@ -198,8 +198,10 @@ constexpr uint32_t kJunkStage = 0xFFFFFFFFu;
 // left one 64 MiB shape 0.5 % slower than without guesses, 3000 2 %.
 constexpr long long kClaimWindow = 1000;
 
-// The ring's first pass issued from guesses, by the whole issuer warp
-// (adjacent rows only).  A CTA that is resident while the previous grid on
+// The ring's first pass issued from guesses, by the whole issuer warp, with
+// bulk copies of runs of adjacent rows, or (kTensorCopies, rows apart) a
+// tensor copy per chunk lying in one block and row copies for a chunk split
+// between two.  A CTA that is resident while the previous grid on
 // the stream still runs would otherwise idle until the grid dependency wait
 // releases, then walk the index chain (boundary index, then request and
 // position, then block-table entry: three dependent loads, 1-1.5 us from L2
@@ -219,15 +221,19 @@ constexpr long long kClaimWindow = 1000;
 //     flight complete it) with the word kJunkStage; the consumers skip those
 //     stages and the issuer copies the first pass again from the resolver's
 //     FIFO, one ring pass later.  The results are the same either way.
-// This warp and the resolver race for the first pass with a compare-and-
-// swap in shared memory, and this warp enters only within kClaimWindow of
-// the resolver's start: a CTA that became resident after the release would
-// finish its guesses too late to gain.  Returns false only when this warp
-// issued the first pass and a guess failed (the same on every lane).
+// This warp claims the first pass with a compare-and-swap in shared memory,
+// and only within kClaimWindow of the resolver's start: a CTA that became
+// resident after the release would finish its guesses too late to gain.
+// With adjacent rows the resolver makes the same claim after its own chain
+// and issues the first pass when it wins; with rows apart it never does, so
+// when this warp does not claim it the issuer starts from the first stage.
+// Returns false only when this warp issued the first pass and a guess
+// failed (the same on every lane).
 // Measured in graph replay against the resolver's issue alone: the
 // headline and every 128 and 256 MiB shape 1.6-1.9 % faster, 1 / 8192 at
 // C = 512 8.5 %; the other 16 and 64 MiB shapes -2.3 .. +0.6 %; calls timed
-// alone unchanged (no earlier grid, so no early CTA).
+// alone unchanged (no earlier grid, so no early CTA).  Rows apart: the
+// headline shape 2.8 % faster, level with adjacent rows.
 template <int S, bool F32, bool kTensorCopies>
 __device__ __noinline__ bool guessed_first_pass(const Params& p, ClusterShared<S>& sh, uint8_t* ring,
                                                 int64_t n0, int64_t units, int k_lo, int kj) {
