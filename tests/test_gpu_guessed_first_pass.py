@@ -247,3 +247,54 @@ def test_rejected_guesses_in_a_multi_layer_call_with_rows_apart(kvc, oracle_mod)
     d["state_cache"] = _rows_apart(case, case.state_bits, 64)
     rejected = _check_chain(kvc, oracle_mod, case, d, layers=3)
     assert rejected > 0
+
+
+@pytest.mark.parametrize("poison", [False, True], ids=["guesses", "poisoned"])
+def test_headline_graph_replay_equals_the_call_alone(kvc, oracle_mod, poison):
+    # The bench times the headline shape (8 requests x 16384 tokens, C = 128)
+    # as back-to-back calls replayed from a CUDA graph, where the next
+    # launch's CTAs start inside the previous one and take the guessed first
+    # pass.  Every replayed call must write exactly the bytes of the call
+    # made alone, which meets the parity bar.
+    case = inputs.headline_case()
+    d = to_device(case)
+    N, n = case.num_outputs, 8
+    stream = torch.cuda.Stream()
+    ws = torch.zeros(kvc.kvc_workspace_bytes(N), dtype=torch.uint8, device="cuda")
+    kvs = [d["kv_cache"].clone() for _ in range(n + 1)]
+    ys = [torch.full((N, 512), float("nan"), dtype=torch.float32, device="cuda") for _ in range(n + 1)]
+
+    def call(i):
+        kvc.c128_256_512_compress(block_size=case.block_size, compress_ratio=case.compress_ratio,
+                                  rms_norm_eps=case.rms_norm_eps, y_out=ys[i], stream=stream,
+                                  workspace=ws, **dict(d, kv_cache=kvs[i]))
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        call(n)                            # the call alone (also warms the library up)
+        stream.synchronize()
+        assert kvc.kvc_get_device_error(stream.cuda_stream) == 0
+        kv_ref, y_ref = kvs[n].cpu().numpy(), ys[n].cpu().numpy()
+        # the launch parameters, the poison setting among them, are fixed
+        # when the graph is captured
+        assert kvc.kvc_selftest_poison_guesses(poison) == 0
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    call(i)
+        finally:
+            assert kvc.kvc_selftest_poison_guesses(False) == 0
+        for k, y in zip(kvs[:n], ys[:n]):  # capturing runs nothing; start from the prefill anyway
+            k.copy_(d["kv_cache"])
+            y.fill_(float("nan"))
+        stream.synchronize()
+        kvc.kvc_selftest_first_pass_rejections(stream.cuda_stream)
+        g.replay()
+        assert kvc.kvc_get_device_error(stream.cuda_stream) == 0
+        rejected = kvc.kvc_selftest_first_pass_rejections(stream.cuda_stream)
+    assert (rejected > 0) if poison else (rejected == 0)
+    for k, y in zip(kvs[:n], ys[:n]):
+        assert np.array_equal(k.cpu().numpy(), kv_ref)
+        assert np.array_equal(y.cpu().numpy().view(np.int32), y_ref.view(np.int32))
+    assert_parity(oracle_mod, case, kv_ref, y_ref)
